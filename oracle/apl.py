@@ -1,0 +1,62 @@
+"""Overlay bitplane format with per-row lookup tables (oracle).
+
+TEST INFRASTRUCTURE ONLY (see oracle/__init__.py).
+
+Source: PagedWeight, "Core components" 1 (Paged Weight representation): the
+weights are held in Any-Precision's overlay bitplane format with associated
+lookup tables; a b-bit view of a block reads its top b bitplanes.
+
+Readings (the pages give no layout):
+  * n = 8 planes per block; plane p holds bit (7 - p) of every 8-bit code, so
+    plane 0 is the most significant and the top-b planes are planes 0..b-1,
+    a contiguous prefix of the storage.
+  * Plane-major layout uint32 [8][N][K/32]; within a plane, row n's word w
+    holds weights k = 32w .. 32w+31, weight k at bit (k mod 32) (LSB first).
+  * Reading the top b planes gives idx_b = sum_{p<b} bit_p << (b-1-p), which
+    equals code >> (8 - b).
+  * Row n's b-bit lookup table holds 2^b fp16 values; the weight is
+    LUT_q[n][idx_q] at the block's committed bitwidth q.
+"""
+import numpy as np
+
+PLANES = 8
+
+
+def pack_bitplanes(codes: np.ndarray) -> np.ndarray:
+    """Encode 8-bit codes [N, K] as 8 bitplanes, uint32 [8, N, K/32]."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    N, K = codes.shape
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    grouped = codes.reshape(N, K // 32, 32)
+    planes = np.zeros((PLANES, N, K // 32), dtype=np.uint32)
+    for p in range(PLANES):
+        bit = ((grouped >> (7 - p)) & 1).astype(np.uint32)   # bit (7-p) of each code
+        for t in range(32):
+            planes[p] |= bit[:, :, t] << np.uint32(t)          # weight 32w+t -> bit t
+    return planes
+
+
+def unpack_top(planes: np.ndarray, b: int) -> np.ndarray:
+    """Read the top b planes back into b-bit indices, uint8 [N, K]."""
+    planes = np.asarray(planes, dtype=np.uint32)
+    if not 1 <= b <= planes.shape[0]:
+        raise ValueError("b out of range")
+    _, N, W = planes.shape
+    k = np.arange(W * 32)
+    word, bit = k // 32, (k % 32).astype(np.uint32)
+    idx = np.zeros((N, W * 32), dtype=np.uint32)
+    for p in range(b):
+        plane_bit = (planes[p][:, word] >> bit) & 1
+        idx = (idx << 1) | plane_bit        # plane 0 ends up as the top index bit
+    return idx.astype(np.uint8)
+
+
+def dequant(planes: np.ndarray, lut_q: np.ndarray, q: int) -> np.ndarray:
+    """Weights of a block at committed bitwidth q: W[n,k] = LUT_q[n][idx_q[n,k]] (fp64)."""
+    lut_q = np.asarray(lut_q)
+    if lut_q.shape[-1] != (1 << q):
+        raise ValueError("LUT width must be 2^q")
+    idx = unpack_top(planes, q)
+    rows = np.arange(idx.shape[0])[:, None]
+    return lut_q[rows, idx].astype(np.float64)
