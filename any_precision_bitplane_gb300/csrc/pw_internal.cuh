@@ -1,0 +1,78 @@
+// Internal declarations shared by the libpw translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "pw.h"
+
+struct pw_page_table {
+  int32_t num_blocks;
+  int device;
+  pw_block_entry* d_entries;  // fixed device address for the table's lifetime
+  int32_t* d_status;          // first device-side error latched by forward calls
+};
+
+namespace pw {
+
+// ---- error reporting (host) ------------------------------------------------
+int fail(int code, const char* fmt, ...);
+int cuda_fail(cudaError_t err, const char* what);
+void clear_error();
+
+// ---- device helpers ----------------------------------------------------------
+__device__ __forceinline__ void latch_status(int32_t* status, int32_t code) {
+  if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ bool supported_q(int q) {
+  return q == 3 || q == 4 || q == 5 || q == 6 || q == 8;
+}
+
+inline bool supported_q_host(int q) { return q == 3 || q == 4 || q == 5 || q == 6 || q == 8; }
+
+// ---- launchers (each returns the launch error) -----------------------------
+cudaError_t launch_pack_bitplanes(const uint8_t* codes, int N, int K, uint32_t* planes,
+                                  cudaStream_t s);
+cudaError_t launch_unpack_top(const uint32_t* planes, int N, int K, int b, uint8_t* idx,
+                              cudaStream_t s);
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids,
+                              float* wts, cudaStream_t s);
+cudaError_t launch_permute(const int32_t* ids, int n_pairs, int E, int32_t* offsets,
+                           int32_t* perm, int32_t* inv, int32_t* status, cudaStream_t s);
+
+constexpr int kMaxCommitPerLaunch = 240;  // keeps the parameter block under 4 KB
+struct CommitBatch {
+  int32_t n;
+  int32_t kind;  // 0 = bitwidth + LUT, 1 = planes + state
+  int32_t ids[kMaxCommitPerLaunch];
+  int32_t ival[kMaxCommitPerLaunch];
+  const void* ptr[kMaxCommitPerLaunch];
+};
+cudaError_t launch_commit(pw_block_entry* entries, const CommitBatch& batch, cudaStream_t s);
+
+// Fused layer, decode path.
+struct LayerArgs {
+  int32_t T, H, I, E, k;
+  const uint16_t* hidden;        // bf16 bits [T][H]
+  const int32_t* topk_ids;       // [T][k]
+  const float* topk_weights;     // [T][k]
+  const pw_block_entry* table;   // [2E]
+  float* out;                    // [T][H]
+  int32_t* status;
+};
+size_t decode_workspace_bytes(const pw_moe_shape& s);
+cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t s);
+int decode_max_pairs();
+int decode_max_experts();
+
+// Fused layer, prefill path.
+size_t prefill_workspace_bytes(const pw_moe_shape& s);
+cudaError_t launch_prefill(const LayerArgs& a, void* ws, cudaStream_t s);
+int prefill_min_pairs(const pw_moe_shape& s);
+
+}  // namespace pw

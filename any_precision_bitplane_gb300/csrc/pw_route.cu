@@ -1,0 +1,184 @@
+// Router (softmax top-k with renormalised weights) and the token-to-expert
+// permutation that groups (token, expert) pairs by expert.
+#include <cfloat>
+#include <climits>
+
+#include "pw_internal.cuh"
+
+namespace pw {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// One warp per token.  Lane l owns experts l, l+32, ... (E <= 1024, so one
+// 32-bit mask per lane marks the experts already taken).  Each of the k rounds
+// is a warp argmax by (logit descending, id ascending); softmax is monotone,
+// so selecting on logits selects on probabilities.  The kept weights are the
+// softmax over the kept logits, which equals the full softmax renormalised.
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits,
+                                                         int T, int E, int k,
+                                                         int32_t* __restrict__ ids,
+                                                         float* __restrict__ wts) {
+  const int lane = threadIdx.x & 31;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  const float* row = logits + static_cast<long long>(t) * E;
+  uint32_t taken = 0;
+  int my_e = -1;
+  float my_v = -INFINITY;
+  for (int r = 0; r < k; ++r) {
+    float best_v = -INFINITY;
+    int best_e = INT_MAX;
+    for (int i = 0, e = lane; e < E; ++i, e += 32) {
+      if ((taken >> i) & 1u) continue;
+      const float v = row[e];
+      if (v > best_v || (v == best_v && e < best_e)) {
+        best_v = v;
+        best_e = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, best_v, off);
+      const int oe = __shfl_xor_sync(kFull, best_e, off);
+      if (ov > best_v || (ov == best_v && oe < best_e)) {
+        best_v = ov;
+        best_e = oe;
+      }
+    }
+    if (best_e == INT_MAX) best_e = -1;  // only NaN logits left
+    if (best_e >= 0 && (best_e & 31) == lane) taken |= 1u << (best_e >> 5);
+    if (lane == r) {
+      my_e = best_e;
+      my_v = best_v;
+    }
+  }
+  const float top = __shfl_sync(kFull, my_v, 0);
+  const float ex = (lane < k && my_e >= 0) ? expf(my_v - top) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+  if (lane < k) {
+    ids[static_cast<long long>(t) * k + lane] = my_e;
+    wts[static_cast<long long>(t) * k + lane] = ex / sum;
+  }
+}
+
+// Single CTA of 8 warps.  Pass 1 counts pairs per expert; a block scan turns
+// the counts into offsets.  Pass 2 walks the pairs in chunks of 256 in
+// ascending order: inside a warp, __match_any_sync gives each pair its rank
+// among same-expert lanes; per-warp counts in shared memory give the rank
+// among earlier warps of the chunk; a running base per expert carries the
+// count of earlier chunks.  Position = offsets[e] + earlier pairs of e, which
+// is the stable order.
+constexpr int kPermThreads = 256;
+constexpr int kPermWarps = kPermThreads / 32;
+
+__global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __restrict__ ids,
+                                                               int n_pairs, int E,
+                                                               int32_t* __restrict__ offsets,
+                                                               int32_t* __restrict__ perm,
+                                                               int32_t* __restrict__ inv,
+                                                               int32_t* status) {
+  extern __shared__ int smem[];
+  int* s_count = smem;                 // [E]
+  int* s_base = s_count + E;           // [E] running position of the next pair of e
+  int* s_wcnt = s_base + E;            // [kPermWarps][E]
+  __shared__ int s_warp_sum[kPermWarps];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+
+  for (int e = tid; e < E; e += kPermThreads) s_count[e] = 0;
+  for (int i = tid; i < kPermWarps * E; i += kPermThreads) s_wcnt[i] = 0;
+  __syncthreads();
+  for (int p = tid; p < n_pairs; p += kPermThreads) {
+    const int e = ids[p];
+    if (e >= 0 && e < E) {
+      atomicAdd(&s_count[e], 1);
+    } else {
+      latch_status(status, PW_ERR_BAD_EXPERT_ID);
+    }
+  }
+  __syncthreads();
+
+  // Exclusive scan of s_count into s_base: each thread owns a contiguous run.
+  const int per = (E + kPermThreads - 1) / kPermThreads;
+  const int lo = min(E, tid * per), hi = min(E, lo + per);
+  int run = 0;
+  for (int e = lo; e < hi; ++e) run += s_count[e];
+  int incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_warp_sum[warp] = incl;
+  __syncthreads();
+  int before = incl - run;
+  for (int w = 0; w < warp; ++w) before += s_warp_sum[w];
+  for (int e = lo; e < hi; ++e) {
+    s_base[e] = before;
+    offsets[e] = before;
+    before += s_count[e];
+  }
+  if (tid == kPermThreads - 1) {
+    int total = 0;
+    for (int w = 0; w < kPermWarps; ++w) total += s_warp_sum[w];
+    offsets[E] = total;
+  }
+  __syncthreads();
+
+  for (int c0 = 0; c0 < n_pairs; c0 += kPermThreads) {
+    const int p = c0 + tid;
+    const int e = (p < n_pairs) ? ids[p] : -1;
+    const bool valid = (e >= 0 && e < E);
+    const int key = valid ? e : -1;
+    const unsigned peers = __match_any_sync(kFull, key);
+    const unsigned lower = peers & ((1u << lane) - 1u);
+    if (valid && lower == 0) s_wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int pos = s_base[e] + __popc(lower);
+      for (int w = 0; w < warp; ++w) pos += s_wcnt[w * E + e];
+      perm[pos] = p;
+      if (inv != nullptr) inv[p] = pos;
+    } else if (p < n_pairs && inv != nullptr) {
+      inv[p] = -1;
+    }
+    __syncthreads();
+    for (int x = tid; x < E; x += kPermThreads) {
+      int add = 0;
+      for (int w = 0; w < kPermWarps; ++w) {
+        add += s_wcnt[w * E + x];
+        s_wcnt[w * E + x] = 0;
+      }
+      s_base[x] += add;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids,
+                              float* wts, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int blocks = (T + 7) / 8;
+  route_topk_kernel<<<blocks, 256, 0, s>>>(logits, T, E, k, ids, wts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const int32_t* ids, int n_pairs, int E, int32_t* offsets,
+                           int32_t* perm, int32_t* inv, int32_t* status, cudaStream_t s) {
+  const size_t smem = sizeof(int) * static_cast<size_t>(E) * (2 + kPermWarps);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  permute_kernel<<<1, kPermThreads, smem, s>>>(ids, n_pairs, E, offsets, perm, inv, status);
+  return cudaGetLastError();
+}
+
+}  // namespace pw

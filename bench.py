@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Throughput of the fused mixed-precision MoE layer (PagedWeight) on GB300.
+
+One step = one pw_moe_forward call over one batch of the workload: every
+routed expert's gate_up and down blocks read at their committed bitwidths
+from the overlay bitplanes + per-row LUTs, SiLU gating, and the weighted
+top-k combine.  Inputs are synthetic and seeded (workloads/), resident in
+HBM before the timed region; L2 is defeated by rotating independent copies
+of the layer (planes, LUTs and page table each), so every step reads its
+weights from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--T T]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+replica of the layer (the layer has no cross-GPU exchange); value sums the
+tokens of all ranks over the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+HBM_FALLBACK_GBS = 6800.0
+KERNEL_SOURCES = ("any_precision_bitplane_gb300/csrc/pw_decode.cu",
+                  "any_precision_bitplane_gb300/csrc/pw_prefill.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--workload", default="qwen15_decode")
+    ap.add_argument("--T", type=int, default=4, help="tokens per step (decode batch)")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the other batch sizes")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, T):
+    """DRAM bytes per forward call from the committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 4 and parts[0] == workload and parts[1] == "T=%d" % T:
+                    if parts[3] == kernel_source_sha():
+                        return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons every 100 ms while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = [r for ts, r in self.rows if t0 - 0.15 <= ts <= t1 + 0.15] or [r for _, r in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = set()
+        sm, mx = [], []
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[3:7]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- native arm
+
+def setup_workload(name, T, device):
+    import torch
+    import any_precision_bitplane_gb300 as pw
+    from any_precision_bitplane_gb300.layer import DeviceLayer
+    from workloads import configs, gen
+
+    cfg = configs.config_by_name(name)
+    layer = gen.make_layer(cfg, 0)
+    base = DeviceLayer(layer, device=device)
+    tok = gen.make_tokens(layer, T)
+    logits = torch.from_numpy(tok.logits).to(device)
+    ids, wts = pw.route_topk(logits, cfg.k)          # the library's router, on the device
+    hidden = torch.from_numpy(tok.hidden_bf16.view(np.int16)).to(device)
+    torch.cuda.synchronize(device)
+    ids_host = ids.cpu().numpy()
+    weight_bytes = base.routed_bytes(ids_host)
+    step_bytes = weight_bytes + T * cfg.H * 2 + T * cfg.k * 8 + T * cfg.H * 4
+    copies = max(2, math.ceil(2 * L2_BYTES / max(weight_bytes, 1)))
+    layers = [base] + [base.clone() for _ in range(copies - 1)]
+    host = {"hidden": tok.hidden_bf16.view(np.int16), "ids": ids_host,
+            "wts": wts.cpu().numpy()}
+    return cfg, layer, layers, hidden, ids, wts, step_bytes, weight_bytes, host
+
+
+def time_device(pw, cfg, layers, hidden, ids, wts, steps, warmup, stream):
+    import torch
+    T = hidden.shape[0]
+    out = torch.empty((T, cfg.H), dtype=torch.float32, device=hidden.device)
+    ws = torch.empty(max(pw.workspace_bytes(T, cfg.H, cfg.I, cfg.E, cfg.k), 256),
+                     dtype=torch.uint8, device=hidden.device)
+    L = len(layers)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            pw.moe_forward(hidden, ids, wts, layers[i % L].table, cfg.I, cfg.E, out=out,
+                           workspace=ws)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps):
+                pw.moe_forward(hidden, ids, wts, layers[i % L].table, cfg.I, cfg.E, out=out,
+                               workspace=ws)
+        g.replay()                     # instantiation/upload, untimed
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        return g, start, stop, out
+
+
+def time_e2e(pw, cfg, layers, host, steps, warmup, device):
+    """Through the public API with host buffers: per step, H2D of the step's
+    inputs from pinned memory, the forward call, D2H of the output."""
+    import torch
+    T = host["hidden"].shape[0]
+    h_hidden = torch.from_numpy(host["hidden"]).pin_memory()
+    h_ids = torch.from_numpy(host["ids"]).pin_memory()
+    h_wts = torch.from_numpy(host["wts"]).pin_memory()
+    h_out = torch.empty((T, cfg.H), dtype=torch.float32).pin_memory()
+    d_hidden = torch.empty_like(h_hidden, device=device)
+    d_ids = torch.empty_like(h_ids, device=device)
+    d_wts = torch.empty_like(h_wts, device=device)
+    d_out = torch.empty((T, cfg.H), dtype=torch.float32, device=device)
+    ws = torch.empty(max(pw.workspace_bytes(T, cfg.H, cfg.I, cfg.E, cfg.k), 256),
+                     dtype=torch.uint8, device=device)
+    L = len(layers)
+
+    def step(i):
+        d_hidden.copy_(h_hidden, non_blocking=True)
+        d_ids.copy_(h_ids, non_blocking=True)
+        d_wts.copy_(h_wts, non_blocking=True)
+        pw.moe_forward(d_hidden, d_ids, d_wts, layers[i % L].table, cfg.I, cfg.E, out=d_out,
+                       workspace=ws)
+        h_out.copy_(d_out, non_blocking=True)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(i)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    bi = h_hidden.numel() * 2 + h_ids.numel() * 4 + h_wts.numel() * 4
+    bo = h_out.numel() * 4
+    return dt, bi, bo
+
+
+def _oracle_setup(name, T):
+    """The oracle's inputs: routing from its router, every block encoded once
+    into bitplanes (storage, done before timing as on the GPU side)."""
+    from oracle import apl, moe
+    from workloads import configs, gen
+    cfg = configs.config_by_name(name)
+    layer = gen.make_layer(cfg, 0)
+    tok = gen.make_tokens(layer, T)
+    ids, w = moe.route_topk(tok.logits, cfg.k)
+    encoded = {}
+    for e in sorted(set(int(x) for x in np.unique(ids))):
+        for m in (0, 1):
+            codes, luts, q = layer.block(e, m)
+            encoded[(e, m)] = (apl.pack_bitplanes(codes), luts[q], q)
+    return cfg, tok, ids, w.astype(np.float32), (lambda e, m: encoded[(e, m)])
+
+
+def cpu_baseline(name, T, budget_s=20.0):
+    """The oracle as it stands, on host cores, over a bounded sample: whole
+    decode batches (stops after ~budget_s or 3 batches)."""
+    from oracle import moe
+    cfg, tok, ids, w, block = _oracle_setup(name, T)
+    done, calls, t0 = 0, 0, time.perf_counter()
+    while True:
+        moe.moe_forward(tok.hidden_bf16, ids, w, block, cfg.E)
+        done += T
+        calls += 1
+        if time.perf_counter() - t0 > budget_s or calls >= 3:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "%d full forward(s) of the T=%d batch: fp64 NumPy in one process "
+                      "(top-q unpack + LUT dequant of every routed block, matmuls, combine; "
+                      "blocks encoded before timing)" % (calls, T)}
+
+
+def native(args):
+    import torch
+    import any_precision_bitplane_gb300 as pw
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    pw.lib()
+    peak, peak_kind = measured_peaks()
+
+    cfg, layer, layers, hidden, ids, wts, step_bytes, weight_bytes, host = \
+        setup_workload(args.workload, args.T, device)
+    stream = torch.cuda.Stream(device)
+    g, start, stop, out = time_device(pw, cfg, layers, hidden, ids, wts, args.steps,
+                                      args.warmup, stream)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        g.replay()
+        stop.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    time.sleep(0.2)
+    sampler.stop()
+    ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    T = args.T
+    tokens_total = T * args.steps * world
+    value = tokens_total / (ms / 1e3)
+    per_launch_s = ms / 1e3 / args.steps
+    achieved = step_bytes / per_launch_s / 1e9
+
+    e2e_dt, bi, bo = time_e2e(pw, cfg, layers, host, args.steps, args.warmup, device)
+    e2e_value = T * args.steps * world / e2e_dt
+
+    sweep = {}
+    if not args.no_sweep and rank == 0 and world == 1:
+        for t2 in cfg.T:
+            if t2 == T:
+                continue
+            c2, _, l2, hd2, id2, w2, sb2, _, _ = setup_workload(args.workload, t2, device)
+            g2, s2, e2, _ = time_device(pw, c2, l2, hd2, id2, w2, args.steps, args.warmup, stream)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                s2.record(stream)
+                g2.replay()
+                e2.record(stream)
+            torch.cuda.synchronize()
+            ms2 = s2.elapsed_time(e2)
+            gbs = sb2 / (ms2 / 1e3 / args.steps) / 1e9
+            sweep["T=%d" % t2] = {"tokens_per_s": t2 * args.steps / (ms2 / 1e3),
+                                  "us_per_step": ms2 * 1e3 / args.steps,
+                                  "GB_per_s": gbs, "frac": gbs / peak,
+                                  "bytes_per_step": sb2}
+            for x in l2:
+                x.close()
+            del g2
+            torch.cuda.empty_cache()
+
+    clocks = sampler.summary(w0, w1)
+    line = {
+        "metric": "MoE-layer tokens/s (decode, Qwen1.5-MoE-A2.7B-shaped layer)",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp32 accumulate (bf16 activations, 3-8 bit LUT weights)",
+        "data": "synthetic (seeded codes, LUTs, bitwidths, hidden states and router logits)",
+        "config": {"workload": "%s: H=%d I=%d E=%d top-%d, T=%d tokens per step" %
+                               (cfg.name, cfg.H, cfg.I, cfg.E, cfg.k, T),
+                   "bitwidths": "q drawn per block from {3,4,5,6,8}",
+                   "l2": "inputs larger than L2: %d rotating layer copies, %.1f MB of routed "
+                         "weights per step" % (len(layers), weight_bytes / 1e6),
+                   "timing": "CUDA events around one CUDA-graph replay of exactly K steps",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "pw_moe_forward decode launch pair (gateup + down)",
+                     "bytes_per_launch": step_bytes,
+                     "traffic": recorded_traffic(args.workload, T)},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if sweep:
+        line["sweep"] = sweep
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, T)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for x in layers:
+        x.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+
+def reference(args):
+    """The CPU oracle on the same workload and metric.  One step = one routed
+    (token, expert) pair of the batch through the oracle (1/k of a token), so
+    that any --steps stays a bounded amount of CPU work."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import moe
+    cfg, tok, ids, w, block = _oracle_setup(args.workload, args.T)
+    T, k = ids.shape
+
+    def step(i):
+        t, j = (i // k) % T, i % k
+        y = moe.expert_outputs(tok.hidden_bf16, ids, block, cfg.E, experts=[int(ids[t, j])],
+                               tokens=[t])
+        return float(w[t, j]) * y[t * k + j]
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = (args.steps / k) / dt
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "MoE-layer tokens/s (decode, Qwen1.5-MoE-A2.7B-shaped layer)",
+        "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "%s: H=%d I=%d E=%d top-%d, T=%d tokens per step" %
+                               (cfg.name, cfg.H, cfg.I, cfg.E, cfg.k, args.T)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "each step: one routed (token, expert) pair of the batch "
+                                   "through the oracle, i.e. 1/%d of a token" % k},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        reference(args)
+    else:
+        native(args)
+
+
+if __name__ == "__main__":
+    main()

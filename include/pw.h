@@ -1,0 +1,237 @@
+/*
+ * pw.h -- C ABI of the PagedWeight fused mixed-precision MoE layer (libpw.so).
+ *
+ * The layer is the one described on the PagedWeight pages:
+ *   - "Core components" 1, Paged Weight representation: experts' weights are
+ *     stored per linear block (layer, expert, module in {gate_up, down}) in
+ *     Any-Precision's overlay bitplane format with lookup tables (LUTs); a
+ *     Weight Page Table tracks each block's committed bitwidth q_i and its page
+ *     state (GPU-resident, CPU-resident or in transfer).
+ *   - "Core components" 3, asynchronous execution and kernel optimisation: a
+ *     fused mixed-precision kernel reads the bitplanes and LUTs directly and
+ *     supports a different bitwidth per linear block inside one fused
+ *     operation; bitwidth commits only take effect at safe boundaries so that
+ *     inference is never interrupted.
+ *
+ * Storage format (the pages give none; this is the library's contract):
+ *   - A block with N rows and K columns (K % 32 == 0) stores 8 bitplanes of
+ *     its 8-bit codes, uint32 [8][N][K/32], plane-major.  Plane p holds bit
+ *     (7 - p) of every code (plane 0 = most significant), so the top q planes
+ *     are the first q planes, a contiguous prefix.  Within a plane, row n's
+ *     word w holds columns 32w..32w+31, column 32w+t at bit t.
+ *   - Reading q planes gives idx_q = code >> (8 - q).  Row n's q-bit LUT holds
+ *     2^q fp16 values, fp16 [N][2^q]; the weight is LUT_q[n][idx_q].
+ *   - Expert e owns block 2e (gate_up, N = 2I rows x K = H: rows 0..I-1 gate,
+ *     rows I..2I-1 up) and block 2e+1 (down, N = H rows x K = I).
+ *   - Supported committed bitwidths: q in {3, 4, 5, 6, 8}.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must be device memory (or managed
+ *     memory) of the current device; they stay owned by the caller.  Host
+ *     pointers are read before the call returns.
+ *   - Work is enqueued on `stream` and is asynchronous; nothing synchronises
+ *     the host unless the comment says so.
+ *   - The return value is a status code (PW_OK = 0).  On failure nothing is
+ *     enqueued and pw_last_error() returns a message (thread-local).  No C++
+ *     exception crosses the ABI.
+ *   - Errors found on the device (an expert id out of range, a page that is
+ *     not GPU-resident) never trap: the offending unit of work is skipped and
+ *     the first such code is latched in the page table's status word, read
+ *     with pw_page_table_status().
+ */
+#ifndef PW_H_
+#define PW_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define PW_OK                     0
+#define PW_ERR_INVALID_ARG        1  /* null pointer, negative size, bad enum        */
+#define PW_ERR_UNSUPPORTED_Q      2  /* q not in {3,4,5,6,8} (or b not in 1..8)      */
+#define PW_ERR_SHAPE              3  /* K % 32 != 0, table size != 2E, size limits   */
+#define PW_ERR_WORKSPACE          4  /* workspace null or smaller than required      */
+#define PW_ERR_PAGE_NOT_RESIDENT  5  /* device: a routed block is not GPU-resident   */
+#define PW_ERR_BAD_EXPERT_ID      6  /* device: topk id outside [0, E)               */
+#define PW_ERR_CUDA               7  /* a CUDA runtime call failed                   */
+#define PW_ERR_TIMEOUT            8  /* a bounded device wait gave up                */
+#define PW_ERR_UNSUPPORTED_DEVICE 9  /* the current device is not sm_103             */
+
+/* ---- page states of the Weight Page Table ------------------------------ */
+#define PW_PAGE_GPU          0  /* planes and LUT are in device memory        */
+#define PW_PAGE_CPU          1  /* offloaded to host memory: not readable     */
+#define PW_PAGE_IN_TRANSFER  2  /* a copy is in flight: not readable          */
+
+/* ---- forward paths ----------------------------------------------------- */
+#define PW_PATH_AUTO     0  /* decode kernels for small token counts, else prefill */
+#define PW_PATH_DECODE   1  /* CUDA-core fused decode kernels                       */
+#define PW_PATH_PREFILL  2  /* dequantise-to-shared-memory tcgen05 GEMM kernels     */
+
+/* One linear block's page-table entry (24 bytes).  PagedWeight, "Core
+ * components" 1: the Weight Page Table keeps each block's committed bitwidth
+ * q_i and page state; this entry adds where the block's planes and its
+ * committed LUT live. */
+typedef struct pw_block_entry {
+  int32_t q;               /* committed bitwidth q_i, in {3,4,5,6,8}                   */
+  int32_t state;           /* PW_PAGE_*                                                */
+  const uint32_t* planes;  /* device: uint32 [>= q][N][K/32], the block's planes      */
+  const uint16_t* lut;     /* device: fp16 [N][2^q], the LUT for the committed q       */
+} pw_block_entry;
+
+/* Shape of one routed-expert layer call. */
+typedef struct pw_moe_shape {
+  int32_t T;  /* tokens (>= 0)                                  */
+  int32_t H;  /* hidden size (> 0, multiple of 32)               */
+  int32_t I;  /* expert intermediate size (> 0, multiple of 32)  */
+  int32_t E;  /* experts (> 0); the page table holds 2E blocks   */
+  int32_t k;  /* experts per token (1..E)                        */
+} pw_moe_shape;
+
+/* Opaque Weight Page Table.  Its entry array sits at one fixed device
+ * address for the table's lifetime, so a CUDA graph that captured a forward
+ * call keeps reading the current commits. */
+typedef struct pw_page_table pw_page_table;
+
+/* Last error message of the calling thread ("" if none). */
+const char* pw_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pw_version(void);
+
+/* ---- bitplane encoding -------------------------------------------------
+ * Encode 8-bit codes into the overlay bitplane format (PagedWeight, "Core
+ * components" 1, APL overlay bitplanes).
+ *   codes  device uint8 [N][K], row-major
+ *   planes device uint32 [8][N][K/32] (output)
+ * Errors: PW_ERR_INVALID_ARG (null, N < 0), PW_ERR_SHAPE (K % 32 != 0 or
+ * K <= 0). */
+int pw_pack_bitplanes(const uint8_t* codes, int32_t N, int32_t K,
+                      uint32_t* planes, cudaStream_t stream);
+
+/* Read a block's top b planes back into b-bit indices, idx = code >> (8-b)
+ * (PagedWeight, "Core components" 1: a b-bit view reads the top b planes).
+ * Exposed so that the bit extraction can be checked bit-exactly.
+ *   planes device uint32 [>= b][N][K/32];  idx device uint8 [N][K] (output)
+ * Errors: PW_ERR_INVALID_ARG, PW_ERR_SHAPE, PW_ERR_UNSUPPORTED_Q (b not in 1..8). */
+int pw_unpack_top(const uint32_t* planes, int32_t N, int32_t K, int32_t b,
+                  uint8_t* idx, cudaStream_t stream);
+
+/* ---- routing -------------------------------------------------------------
+ * Router: softmax over E logits, top-k experts (ties to the lower id), the k
+ * kept probabilities renormalised to sum to 1.  The pages describe routing
+ * only through the routing mass the planner tracks (PagedWeight, "Core
+ * components" 2, online routing statistics); the layer itself consumes its
+ * output.
+ *   logits       device float [T][E]
+ *   topk_ids     device int32 [T][k]  (output, descending probability)
+ *   topk_weights device float [T][k]  (output)
+ * Limits: 1 <= k <= E <= 1024 and k <= 32.  Errors: PW_ERR_INVALID_ARG, PW_ERR_SHAPE. */
+int pw_route_topk(const float* logits, int32_t T, int32_t E, int32_t k,
+                  int32_t* topk_ids, float* topk_weights, cudaStream_t stream);
+
+/* Token-to-expert permutation (the dispatch step of the fused layer,
+ * PagedWeight "Core components" 3).  Pair p = t*k + j goes to expert
+ * topk_ids[t][j]; pairs are grouped by expert, ascending p inside an expert.
+ *   topk_ids device int32 [T][k]
+ *   offsets  device int32 [E+1] (output): expert e owns perm[offsets[e] .. offsets[e+1])
+ *   perm     device int32 [T*k] (output): pair ids in grouped order
+ *   inv      device int32 [T*k] (output, may be NULL): inv[perm[r]] = r
+ * Limits: E <= 1024.  An id outside [0, E) latches PW_ERR_BAD_EXPERT_ID in
+ * *status_out (device int32, may be NULL) and that pair is dropped (it then
+ * appears in no expert's range and its inv entry is -1). */
+int pw_permute(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
+               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* status_out,
+               cudaStream_t stream);
+
+/* ---- Weight Page Table ----------------------------------------------------
+ * PagedWeight, "Core components" 1 (Weight Page Table: committed bitwidth q_i
+ * and page state per linear block) and 3 (bitwidth commits applied only at a
+ * safe boundary).
+ *
+ * Create a table of num_blocks entries from host_init (host array).  Allocates
+ * device memory and synchronises the current device once.  Errors:
+ * PW_ERR_INVALID_ARG, PW_ERR_UNSUPPORTED_Q, PW_ERR_CUDA. */
+int pw_page_table_create(int32_t num_blocks, const pw_block_entry* host_init,
+                         pw_page_table** out);
+
+/* Free a table (synchronises the device first).  NULL is accepted. */
+int pw_page_table_destroy(pw_page_table* table);
+
+/* Recommit: for i < n, block block_ids[i] takes bitwidth new_q[i] and reads
+ * the LUT at new_lut[i] (a device pointer to fp16 [N][2^new_q]).  The update
+ * is a kernel enqueued on `stream` (host arrays are passed by value), so a
+ * forward call enqueued later on the same stream sees the new bitwidths and
+ * one enqueued earlier sees the old ones: the stream order is the safe
+ * boundary.  The planes pointer is unchanged: lowering q only stops reading
+ * the tail planes.  Errors: PW_ERR_INVALID_ARG (n < 0, id out of range, null
+ * lut), PW_ERR_UNSUPPORTED_Q. */
+int pw_page_table_commit(pw_page_table* table, int32_t n, const int32_t* block_ids,
+                         const int32_t* new_q, const uint16_t* const* new_lut,
+                         cudaStream_t stream);
+
+/* Move pages: for i < n, block block_ids[i] reads its planes from planes[i]
+ * (device pointer) and takes page state states[i] (PW_PAGE_*).  Stream-ordered
+ * like pw_page_table_commit.  A forward call skips every routed block whose
+ * state is not PW_PAGE_GPU and latches PW_ERR_PAGE_NOT_RESIDENT. */
+int pw_page_table_set_pages(pw_page_table* table, int32_t n, const int32_t* block_ids,
+                            const uint32_t* const* planes, const int32_t* states,
+                            cudaStream_t stream);
+
+/* Copy the current entries to host_out[num_blocks] (host).  Synchronises `stream`. */
+int pw_page_table_read(const pw_page_table* table, pw_block_entry* host_out,
+                       cudaStream_t stream);
+
+/* Number of entries. */
+int32_t pw_page_table_size(const pw_page_table* table);
+
+/* Read the device status word latched by forward calls into *host_status
+ * (PW_OK or the first device-side error) and clear it if reset != 0.
+ * Synchronises `stream`. */
+int pw_page_table_status(pw_page_table* table, int32_t* host_status, int32_t reset,
+                         cudaStream_t stream);
+
+/* ---- the fused layer ------------------------------------------------------
+ * Bytes of device workspace a forward call of this shape needs. */
+int pw_workspace_bytes(const pw_moe_shape* shape, size_t* bytes);
+
+/* The fused mixed-precision MoE expert layer (PagedWeight, "Core components"
+ * 3): for every token t,
+ *   out[t] = sum_j topk_weights[t][j] * y_{e}(x_t),   e = topk_ids[t][j],
+ *   y_e(x) = (SiLU(x W_gate,e^T) * (x W_up,e^T)) W_down,e^T,
+ * where every weight is LUT_q[n][code >> (8-q)] read from the block's top q
+ * bitplanes at the q committed in `table` when the call runs on the stream.
+ *   hidden       device bf16 [T][H] (raw bits), row-major
+ *   topk_ids     device int32 [T][k]
+ *   topk_weights device float [T][k]
+ *   table        page table with 2E entries
+ *   out          device float [T][H] (output, overwritten)
+ *   workspace    device scratch of >= pw_workspace_bytes(shape) bytes, 256-byte
+ *                aligned; it must not be in use by another call in flight
+ * The call allocates nothing and never synchronises the host; it can be
+ * captured in a CUDA graph.  Errors: PW_ERR_INVALID_ARG, PW_ERR_SHAPE,
+ * PW_ERR_WORKSPACE, PW_ERR_UNSUPPORTED_DEVICE, PW_ERR_CUDA. */
+int pw_moe_forward(const pw_moe_shape* shape, const void* hidden, const int32_t* topk_ids,
+                   const float* topk_weights, const pw_page_table* table, float* out,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* pw_moe_forward with an explicit path (PW_PATH_*); PW_PATH_AUTO is what
+ * pw_moe_forward uses.  Both paths compute the same function. */
+int pw_moe_forward_path(const pw_moe_shape* shape, const void* hidden, const int32_t* topk_ids,
+                        const float* topk_weights, const pw_page_table* table, float* out,
+                        void* workspace, size_t workspace_bytes, int32_t path,
+                        cudaStream_t stream);
+
+/* Token count from which PW_PATH_AUTO takes the prefill path for a shape
+ * (T*k pairs >= this value). */
+int32_t pw_prefill_min_pairs(const pw_moe_shape* shape);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PW_H_ */

@@ -23,17 +23,20 @@ PLANES = 8
 
 
 def pack_bitplanes(codes: np.ndarray) -> np.ndarray:
-    """Encode 8-bit codes [N, K] as 8 bitplanes, uint32 [8, N, K/32]."""
+    """Encode 8-bit codes [N, K] as 8 bitplanes, uint32 [8, N, K/32].
+
+    np.packbits with little bit order puts column 32w+t at bit t of word w
+    once the bytes are read as little-endian uint32.
+    """
     codes = np.asarray(codes, dtype=np.uint8)
     N, K = codes.shape
     if K % 32:
         raise ValueError("K must be a multiple of 32")
-    grouped = codes.reshape(N, K // 32, 32)
-    planes = np.zeros((PLANES, N, K // 32), dtype=np.uint32)
+    planes = np.empty((PLANES, N, K // 32), dtype=np.uint32)
     for p in range(PLANES):
-        bit = ((grouped >> (7 - p)) & 1).astype(np.uint32)   # bit (7-p) of each code
-        for t in range(32):
-            planes[p] |= bit[:, :, t] << np.uint32(t)          # weight 32w+t -> bit t
+        bit = (codes >> (7 - p)) & 1                            # plane p = bit (7-p)
+        packed = np.packbits(bit, axis=1, bitorder="little")    # [N, K/8] bytes
+        planes[p] = np.ascontiguousarray(packed).view("<u4")
     return planes
 
 
@@ -43,13 +46,12 @@ def unpack_top(planes: np.ndarray, b: int) -> np.ndarray:
     if not 1 <= b <= planes.shape[0]:
         raise ValueError("b out of range")
     _, N, W = planes.shape
-    k = np.arange(W * 32)
-    word, bit = k // 32, (k % 32).astype(np.uint32)
-    idx = np.zeros((N, W * 32), dtype=np.uint32)
+    idx = np.zeros((N, W * 32), dtype=np.uint8)
     for p in range(b):
-        plane_bit = (planes[p][:, word] >> bit) & 1
+        as_bytes = np.ascontiguousarray(planes[p]).astype("<u4").view(np.uint8)
+        plane_bit = np.unpackbits(as_bytes, axis=1, bitorder="little")  # column k = bit k%32 of word k/32
         idx = (idx << 1) | plane_bit        # plane 0 ends up as the top index bit
-    return idx.astype(np.uint8)
+    return idx
 
 
 def dequant(planes: np.ndarray, lut_q: np.ndarray, q: int) -> np.ndarray:

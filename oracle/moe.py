@@ -21,7 +21,7 @@ Readings (the pages do not write the layer out):
 All floating point here is fp64; bf16 hidden states and fp16 LUT values are
 widened exactly.
 """
-from typing import Callable, Optional, Sequence, Tuple
+from typing import Callable, Dict, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -82,36 +82,50 @@ def expert_mlp(x: np.ndarray, w_gu: np.ndarray, w_dn: np.ndarray) -> np.ndarray:
 BlockFn = Callable[[int, int], Tuple[np.ndarray, np.ndarray, int]]
 
 
-def moe_forward(hidden_bf16: np.ndarray, topk_ids: np.ndarray, topk_weights: np.ndarray,
-                block: BlockFn, E: int, tokens: Optional[Sequence[int]] = None) -> np.ndarray:
-    """The layer output, fp64 [T, H] (or [len(tokens), H] for a token subset).
+def expert_outputs(hidden_bf16: np.ndarray, topk_ids: np.ndarray, block: BlockFn, E: int,
+                   experts: Optional[Sequence[int]] = None,
+                   tokens: Optional[Sequence[int]] = None) -> Dict[int, np.ndarray]:
+    """y_e(x_t) (fp64 [H]) for every routed pair p = t*k + j, keyed by p.
 
     block(e, m) returns (planes uint32 [8, N, K/32], lut_q fp16 [N, 2^q], q)
     for block 2e+m (m = 0 gate_up, m = 1 down), as the page table commits it.
+    `experts` / `tokens` restrict the pairs computed (default: all).
     """
     x = bf16_to_float64(hidden_bf16)
     T, k = topk_ids.shape
-    wts = np.asarray(topk_weights, dtype=np.float64)
     offsets, perm, _ = permute(topk_ids, E)
     wanted = np.ones(T, bool) if tokens is None else np.isin(np.arange(T), tokens)
     y_pair = {}
-    for e in range(E):
+    for e in (range(E) if experts is None else experts):
         pairs = [int(p) for p in perm[offsets[e]:offsets[e + 1]] if wanted[p // k]]
         if not pairs:
             continue
-        planes_gu, lut_gu, q_gu = block(e, 0)
-        planes_dn, lut_dn, q_dn = block(e, 1)
-        w_gu = dequant(planes_gu, lut_gu, q_gu)
-        w_dn = dequant(planes_dn, lut_dn, q_dn)
+        w_gu = dequant(*block(e, 0))
+        w_dn = dequant(*block(e, 1))
         y = expert_mlp(x[[p // k for p in pairs]], w_gu, w_dn)
         for r, p in enumerate(pairs):
             y_pair[p] = y[r]
-    rows = np.flatnonzero(wanted)
-    out = np.zeros((rows.size, x.shape[1]), dtype=np.float64)
+    return y_pair
+
+
+def combine(y_pair: Dict[int, np.ndarray], topk_weights: np.ndarray, H: int,
+            tokens: Optional[Sequence[int]] = None) -> np.ndarray:
+    """out[t] = sum_j w_tj * y_pair[t*k + j], summed in j order (fp64)."""
+    wts = np.asarray(topk_weights, dtype=np.float64)
+    T, k = wts.shape
+    rows = np.arange(T) if tokens is None else np.asarray(sorted(tokens))
+    out = np.zeros((rows.size, H), dtype=np.float64)
     for i, t in enumerate(rows):
         for j in range(k):
-            out[i] += wts[t, j] * y_pair[t * k + j]
+            out[i] += wts[t, j] * y_pair[int(t) * k + j]
     return out
+
+
+def moe_forward(hidden_bf16: np.ndarray, topk_ids: np.ndarray, topk_weights: np.ndarray,
+                block: BlockFn, E: int, tokens: Optional[Sequence[int]] = None) -> np.ndarray:
+    """The layer output, fp64 [T, H] (or [len(tokens), H] for a token subset)."""
+    y_pair = expert_outputs(hidden_bf16, topk_ids, block, E, tokens=tokens)
+    return combine(y_pair, topk_weights, hidden_bf16.shape[1], tokens=tokens)
 
 
 def rel_l2(got: np.ndarray, ref: np.ndarray) -> float:
