@@ -73,6 +73,7 @@ _SIGNATURES = {
     "pw_moe_forward": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _c.c_size_t, _P]),
     "pw_moe_forward_path": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _c.c_size_t, _I32, _P]),
     "pw_prefill_min_pairs": (_I32, [_P]),
+    "pw_moe_forward_noalloc": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -270,4 +271,20 @@ def moe_forward(hidden, topk_ids, topk_weights, table, I, E, out=None, workspace
                                      _ptr(topk_weights), table.handle, _ptr(out),
                                      _ptr(workspace), workspace.numel(), int(path),
                                      _stream(stream)), "pw_moe_forward")
+    return out
+
+
+def moe_forward_noalloc(hidden, topk_ids, topk_weights, table, I, E, out=None, stream=None):
+    """moe_forward without a workspace: the library's fixed static scratch is
+    used instead (decode path; shapes whose scratch exceeds it raise)."""
+    _need_cuda(hidden, topk_ids, topk_weights)
+    T, H = hidden.shape
+    k = topk_ids.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=hidden.device)
+    _need_cuda(out)
+    s = MoeShape(T, H, I, E, k)
+    _check(lib().pw_moe_forward_noalloc(ctypes.byref(s), _ptr(hidden), _ptr(topk_ids),
+                                        _ptr(topk_weights), table.handle, _ptr(out),
+                                        _stream(stream)), "pw_moe_forward_noalloc")
     return out

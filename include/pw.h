@@ -230,6 +230,35 @@ int pw_moe_forward_path(const pw_moe_shape* shape, const void* hidden, const int
  * (T*k pairs >= this value). */
 int32_t pw_prefill_min_pairs(const pw_moe_shape* shape);
 
+/* ---- the fused layer without a workspace ------------------------------------
+ * The PagedWeight pages have no counterpart to this entry point; it is a
+ * service for callers that cannot allocate device memory: a plugin whose
+ * enqueue hook only receives its input and output buffers, a runtime that
+ * fixes its memory budget at start-up and allows no allocation afterwards, or
+ * code where a cudaMalloc would synchronise the device or break a capture.
+ *
+ * Same function and arguments as pw_moe_forward on the decode path, minus the
+ * workspace: the scratch lives in one static device array of 8 MiB inside
+ * libpw (every GPU that loads the library keeps those 8 MiB until the process
+ * exits).  The caller still passes inputs and outputs.
+ *   - Shapes whose decode scratch, 4*T*k*(I + H) bytes plus 4*H/32 rounded
+ *     up to 256-byte sections, exceeds 8 MiB are rejected with
+ *     PW_ERR_WORKSPACE (use pw_moe_forward with a workspace instead), as
+ *     are shapes beyond the decode path's limits (PW_ERR_SHAPE).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - The call allocates nothing: no cudaMalloc, no cudaFree.  Each call
+ *     zeroes the counters it needs and writes every other scratch byte before
+ *     reading it, so nothing is carried over from an earlier call.
+ *   - All calls on a device share the one array: calls that can overlap on
+ *     the GPU (different streams without ordering) race on it and produce
+ *     wrong results.  Order them on one stream.
+ * Errors: as pw_moe_forward, plus PW_ERR_WORKSPACE for shapes over the limit. */
+int pw_moe_forward_noalloc(const pw_moe_shape* shape, const void* hidden,
+                           const int32_t* topk_ids, const float* topk_weights,
+                           const pw_page_table* table, float* out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
