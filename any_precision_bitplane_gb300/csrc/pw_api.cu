@@ -90,6 +90,8 @@ int forward_impl(const pw_moe_shape* shape, const void* hidden, const int32_t* t
                   decode_max_experts());
     e = launch_decode(a, workspace, stream);
   } else {
+    if (!prefill_shape_ok(s))
+      return fail(PW_ERR_SHAPE, "prefill path needs H %% 128 == 0, I %% 64 == 0 and E <= 1024");
     e = launch_prefill(a, workspace, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");

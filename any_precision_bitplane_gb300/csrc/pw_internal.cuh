@@ -74,5 +74,6 @@ int decode_max_experts();
 size_t prefill_workspace_bytes(const pw_moe_shape& s);
 cudaError_t launch_prefill(const LayerArgs& a, void* ws, cudaStream_t s);
 int prefill_min_pairs(const pw_moe_shape& s);
+bool prefill_shape_ok(const pw_moe_shape& s);  // H % 128 == 0, I % 64 == 0, E <= 1024
 
 }  // namespace pw
