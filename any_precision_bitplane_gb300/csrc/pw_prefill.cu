@@ -242,6 +242,16 @@ __device__ __forceinline__ bool tile_usable(Mode mode, const GemmArgs& a, int e)
   return true;
 }
 
+// Latch why a tile of expert e cannot be computed (first error wins).
+__device__ void report_unusable(Mode mode, const GemmArgs& a, int e) {
+  const pw_block_entry ent = a.table[2 * e + (mode == kGateUp ? 0 : 1)];
+  const pw_block_entry gu = a.table[2 * e];
+  if (ent.state != PW_PAGE_GPU || gu.state != PW_PAGE_GPU)
+    latch_status(a.status, PW_ERR_PAGE_NOT_RESIDENT);
+  else
+    latch_status(a.status, PW_ERR_UNSUPPORTED_Q);
+}
+
 // ---------------------------------------------------------------- dequant
 
 // Thread r: fill A-stage row r with the 64 weights of k-step s.
@@ -424,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos0 = a.offsets[tile.e] + tile.n * BN;
       const int ntok = min(BN, a.offsets[tile.e + 1] - pos0);
       const bool usable = tile_usable(mode, a, tile.e);
+      if (!usable && tid == 0) report_unusable(mode, a, tile.e);
       if (usable) {
         const pw_block_entry ent = a.table[2 * tile.e + (mode == kGateUp ? 0 : 1)];
         switch (ent.q) {

@@ -68,6 +68,17 @@ def measured_peaks():
         return HBM_FALLBACK_GBS, "fallback"
 
 
+def tensor_peak():
+    """Dense fp16 tensor peak for a kernel timed alone: the measured bf16 burst
+    figure (fp16 and bf16 have the same nominal dense rate), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst, fp16 = bf16 nominal)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def kernel_source_sha():
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -276,6 +287,49 @@ def cpu_baseline(name, T, budget_s=20.0):
                       "blocks encoded before timing)" % (calls, T)}
 
 
+def prefill_section(pw, device, steps=5, warmup=2):
+    """Mixtral-shaped prefill (4096 tokens, top-2 of 8 experts, H=4096,
+    I=14336): the dequantise-to-shared-memory tcgen05 path."""
+    import torch
+    from any_precision_bitplane_gb300.layer import DeviceLayer
+    from workloads import configs, gen
+    cfg = configs.config_by_name("mixtral_prefill")
+    T = cfg.T[0]
+    layer = gen.make_layer(cfg, 0)
+    dl = DeviceLayer(layer, device=device)
+    tok = gen.make_tokens(layer, T)
+    ids, wts = pw.route_topk(torch.from_numpy(tok.logits).to(device), cfg.k)
+    hidden = torch.from_numpy(tok.hidden_bf16.view(np.int16)).to(device)
+    out = torch.empty((T, cfg.H), dtype=torch.float32, device=device)
+    ws = torch.empty(pw.workspace_bytes(T, cfg.H, cfg.I, cfg.E, cfg.k), dtype=torch.uint8,
+                     device=device)
+    for _ in range(warmup):
+        pw.moe_forward(hidden, ids, wts, dl.table, cfg.I, cfg.E, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(steps):
+        pw.moe_forward(hidden, ids, wts, dl.table, cfg.I, cfg.E, out=out, workspace=ws)
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / steps
+    flops = 2.0 * T * cfg.k * (cfg.H * 2 * cfg.I + cfg.I * cfg.H)
+    peak, kind = tensor_peak()
+    tflops = flops / (ms / 1e3) / 1e12
+    dl.close()
+    del ws
+    torch.cuda.empty_cache()
+    return {"workload": "%s: H=%d I=%d E=%d top-%d, T=%d" % (cfg.name, cfg.H, cfg.I, cfg.E,
+                                                            cfg.k, T),
+            "tokens_per_s": T / (ms / 1e3), "ms_per_step": ms, "steps": steps,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
+                         "unit": "TFLOP/s", "frac": tflops / peak, "peak_kind": kind,
+                         "flops_per_step": flops,
+                         "kernel": "whole prefill call (permute, gather, gate_up and down "
+                                   "dequant+tcgen05 GEMMs, combine)"}}
+
+
 def native(args):
     import torch
     import any_precision_bitplane_gb300 as pw
@@ -348,6 +402,10 @@ def native(args):
             del g2
             torch.cuda.empty_cache()
 
+    prefill = None
+    if not args.no_sweep and rank == 0 and world == 1:
+        prefill = prefill_section(pw, device)
+
     clocks = sampler.summary(w0, w1)
     line = {
         "metric": "MoE-layer tokens/s (decode, Qwen1.5-MoE-A2.7B-shaped layer)",
@@ -381,6 +439,8 @@ def native(args):
     }
     if sweep:
         line["sweep"] = sweep
+    if prefill is not None:
+        line["prefill"] = prefill
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, T)
     if rank == 0:
