@@ -124,11 +124,11 @@ def _need_cuda(*ts):
 # ---------------------------------------------------------------- bitplanes
 
 def pack_bitplanes(codes, planes=None, stream=None):
-    """codes uint8 [N, K] -> planes int32 [8, N, K/32] (raw uint32 bits)."""
+    """codes uint8 [N, K] -> planes int32 [8, K/32, N] (raw uint32 bits)."""
     _need_cuda(codes)
     N, K = codes.shape
     if planes is None:
-        planes = torch.empty((8, N, K // 32), dtype=torch.int32, device=codes.device)
+        planes = torch.empty((8, K // 32, N), dtype=torch.int32, device=codes.device)
     _need_cuda(planes)
     _check(lib().pw_pack_bitplanes(_ptr(codes), N, K, _ptr(planes), _stream(stream)),
            "pw_pack_bitplanes")

@@ -8,16 +8,21 @@
 //           q planes of gate rows i and up rows I+i, rebuild the q-bit codes,
 //           look them up in each row's LUT, dot with the expert's gathered
 //           hidden rows (fp32), then h = SiLU(g) * u -> workspace.
-//   down:   per (routed expert e, tile of 32 down rows): same bitplane/LUT
+//   down:   per (routed expert e, tile of 64 down rows): same bitplane/LUT
 //           read at the down block's q, dot with h -> y for each of e's pairs
 //           (workspace).  The last CTA to finish a row tile (a per-tile
 //           arrival counter) combines out[t] = sum_j w_tj * y[t*k + j] over
 //           the tile in j order, so the output is deterministic.
 //
-// Layout of work inside a CTA: lane L owns row (row0 + L) of the tile, so each
-// lane reads its own row's LUT from a lane-private shared-memory column
-// (entry v of lane L at word v*32 + L: bank L, never a conflict); the 8 warps
-// split the K columns and their partial sums meet in shared memory.
+// Work inside a CTA: lane L owns rows (row0 + L) and (row0' + L) of the tile;
+// the 8 warps split the K columns and their partial sums meet in shared
+// memory.  Per 32 columns a lane loads one word of each of the top q planes
+// per row (a word column of consecutive rows is contiguous, so a warp's load
+// is one 128-byte line), turns the q words into 32 index bytes with a byte
+// transpose and an 8x8 bit-matrix transpose, and looks each index up in its
+// row's LUT, which sits in a lane-private shared-memory column: one byte
+// permute forms the address (index * 256 + slot * 128 + lane * 4), and every
+// lookup of lane L hits bank L.
 //
 // Each CTA finds its expert itself from topk_ids (count, pick the slot-th
 // routed expert, list its pairs in ascending pair order), so no separate
@@ -32,46 +37,46 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kRows = 32;           // rows (gate/up pairs, or down rows) per CTA
-constexpr int kTokGroup = 8;        // tokens per pass over the weights
-constexpr int kChunkWords = 8;      // columns staged per activation chunk: 256
-constexpr int kChunkCols = kChunkWords * 32;
+constexpr int kPairsPerTile = 32;   // gate_up tile: 32 gate rows + their 32 up rows
+constexpr int kDownRows = 64;       // down tile: two 32-row groups
+constexpr int kTG = 4;              // tokens per pass over the weights
+constexpr int kCW = 4;              // words per staged activation chunk
+constexpr int kCC = kCW * 32;       // columns per staged activation chunk
 constexpr int kMaxPairs = 4096;     // T*k limit of this path
 constexpr int kMaxExperts = 1024;
 
-struct Smem {
-  // sizes in 4-byte words
-  static constexpr int count = kMaxExperts;
-  static constexpr int pairs = kMaxPairs;
-  static constexpr int misc = 8;
-  static constexpr int lut = 2 * 256 * 32;
-  static constexpr int act = kWarps * kTokGroup * kChunkCols;
-  static constexpr int red = kWarps * kTokGroup * 2 * 32;
-  static constexpr int total = count + pairs + misc + lut + act + red;
-};
-constexpr size_t kSmemBytes = sizeof(float) * Smem::total;
+// Shared memory (bytes).  The LUT region comes first: entry v of row slot g
+// for lane L sits at byte v*256 + g*128 + L*4 (fp32), so a lane's lookups
+// always hit bank L and one byte permute turns an 8-bit index into the offset.
+constexpr int kLutBytes = 256 * 256;
+constexpr int kActBytes = kWarps * kTG * kCC * 4;
+constexpr int kRedBytes = kWarps * kTG * 2 * 32 * 4;
+constexpr int kCountBytes = kMaxExperts * 4;
+constexpr int kPairBytes = kMaxPairs * 4;
+constexpr int kOffAct = kLutBytes;
+constexpr int kOffRed = kOffAct + kActBytes;
+constexpr int kOffCount = kOffRed + kRedBytes;
+constexpr int kOffPairs = kOffCount + kCountBytes;
+constexpr int kOffMisc = kOffPairs + kPairBytes;
+constexpr size_t kSmemBytes = kOffMisc + 64;
 
 struct SmemPtrs {
+  unsigned char* lut;
+  float* act;
+  float* red;
   int* count;
   int* pairs;
   int* misc;
-  float* lut;
-  float* act;
-  float* red;
 };
 
-__device__ __forceinline__ SmemPtrs carve(void* base) {
+__device__ __forceinline__ SmemPtrs carve(unsigned char* base) {
   SmemPtrs s;
-  int* p = static_cast<int*>(base);
-  s.count = p;
-  p += Smem::count;
-  s.pairs = p;
-  p += Smem::pairs;
-  s.misc = p;
-  p += Smem::misc;
-  s.lut = reinterpret_cast<float*>(p);
-  s.act = s.lut + Smem::lut;
-  s.red = s.act + Smem::act;
+  s.lut = base;
+  s.act = reinterpret_cast<float*>(base + kOffAct);
+  s.red = reinterpret_cast<float*>(base + kOffRed);
+  s.count = reinterpret_cast<int*>(base + kOffCount);
+  s.pairs = reinterpret_cast<int*>(base + kOffPairs);
+  s.misc = reinterpret_cast<int*>(base + kOffMisc);
   return s;
 }
 
@@ -149,67 +154,138 @@ __device__ Route route_slot(const LayerArgs& a, int slot, const SmemPtrs& s, boo
   return r;
 }
 
-// Lane-private LUT columns for R row groups: s.lut[(g * 2^Q + v) * 32 + L] =
-// LUT_Q[row0_g + L][v] as fp32.  Each thread moves 8 fp16 entries (16 bytes).
+// LUT rows of the tile into the lane-private layout: row slot g, lane L,
+// entry v -> byte v*256 + g*128 + L*4, as fp32.  Each thread moves 8 fp16
+// entries (16 bytes); the stores of a warp hit 32 different banks.
 template <int Q, int R>
 __device__ __forceinline__ void load_luts(const uint16_t* lut, const int (&row0)[R],
                                           const SmemPtrs& s) {
   constexpr int kEnt = 1 << Q;
   constexpr int kVecPerRow = kEnt / 8;
-  for (int g = 0; g < R; ++g) {
-    for (int i = threadIdx.x; i < kRows * kVecPerRow; i += kThreads) {
-      const int L = i & 31, vec = i >> 5;
-      const uint4 raw = *reinterpret_cast<const uint4*>(
-          lut + static_cast<long long>(row0[g] + L) * kEnt + vec * 8);
-      const __half* h = reinterpret_cast<const __half*>(&raw);
-      float* dst = s.lut + (g * kEnt + vec * 8) * 32 + L;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) dst[j * 32] = __half2float(h[j]);
+  for (int g = 0; g < R; ++g) {
+    for (int i = threadIdx.x; i < 32 * kVecPerRow; i += kThreads) {
+      const int L = i & 31, vec = i >> 5;
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+          lut + static_cast<long long>(row0[g] + L) * kEnt + vec * 8));
+      const __half* h = reinterpret_cast<const __half*>(&raw);
+      unsigned char* dst = s.lut + (vec * 8) * 256 + g * 128 + L * 4;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) *reinterpret_cast<float*>(dst + j * 256) = __half2float(h[j]);
     }
   }
 }
 
-// Partial dot products of this lane's R rows over the warp's column range,
-// for NT tokens whose activations the loader stages per 256-column chunk.
+// Byte transpose of four 32-bit words: out[b] = {a0.byte b, a1.byte b,
+// a2.byte b, a3.byte b}.
+__device__ __forceinline__ void byte_transpose4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                uint32_t (&out)[4]) {
+  const uint32_t t0 = __byte_perm(a0, a1, 0x5140), t1 = __byte_perm(a0, a1, 0x7362);
+  const uint32_t t2 = __byte_perm(a2, a3, 0x5140), t3 = __byte_perm(a2, a3, 0x7362);
+  out[0] = __byte_perm(t0, t2, 0x5410);
+  out[1] = __byte_perm(t0, t2, 0x7632);
+  out[2] = __byte_perm(t1, t3, 0x5410);
+  out[3] = __byte_perm(t1, t3, 0x7632);
+}
+
+// Transpose of the 8x8 bit matrix held in (lo, hi): byte r = matrix row r,
+// bit c = column c  ->  byte c = column c, bit r = row r.  Three delta swaps.
+__device__ __forceinline__ void bit_transpose8(uint32_t& lo, uint32_t& hi) {
+  uint32_t t;
+  t = (lo ^ (lo >> 7)) & 0x00AA00AAu; lo ^= t ^ (t << 7);
+  t = (hi ^ (hi >> 7)) & 0x00AA00AAu; hi ^= t ^ (t << 7);
+  t = (lo ^ (lo >> 14)) & 0x0000CCCCu; lo ^= t ^ (t << 14);
+  t = (hi ^ (hi >> 14)) & 0x0000CCCCu; hi ^= t ^ (t << 14);
+  t = (lo ^ (hi << 4)) & 0xF0F0F0F0u; lo ^= t; hi ^= t >> 4;
+}
+
+// Q plane words of one row (P[0] = most significant plane) covering 32
+// columns -> the q-bit index of every column, one per byte: byte j of ib[m]
+// is the index of column 4m + j.  Plane p feeds bit (Q-1-p) of the index;
+// for Q <= 4 half of the matrix is zero and the compiler folds it away.
+template <int Q>
+__device__ __forceinline__ void planes_to_index_bytes(const uint32_t (&P)[Q], uint32_t (&ib)[8]) {
+  uint32_t r[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = (i < Q) ? P[Q - 1 - i] : 0u;
+  uint32_t A[4], B[4];
+  byte_transpose4(r[0], r[1], r[2], r[3], A);
+  byte_transpose4(r[4], r[5], r[6], r[7], B);
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    uint32_t lo = A[b], hi = B[b];
+    bit_transpose8(lo, hi);
+    ib[2 * b] = lo;
+    ib[2 * b + 1] = hi;
+  }
+}
+
+__device__ __forceinline__ float lane4(const float4& v, int j) {
+  return (j == 0) ? v.x : (j == 1) ? v.y : (j == 2) ? v.z : v.w;
+}
+
+// Partial dot products of this lane's R rows over the warp's words
+// [kw_lo, kw_hi), for NT tokens whose activations `load_chunk` stages per
+// kCW-word chunk.  Plane words are loaded one word column ahead.
 template <int Q, int R, int NT, class Loader>
-__device__ __forceinline__ void rows_dot(const uint32_t* planes, long long plane_stride,
-                                         const int (&row)[R], int kw_lo, int kw_hi, int KW,
+__device__ __forceinline__ void rows_dot(const uint32_t* planes, long long plane_stride, int N,
+                                         const int (&row)[R], int kw_lo, int kw_hi,
                                          const SmemPtrs& s, const Loader& load_chunk,
                                          float (&acc)[R][NT]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float* act = s.act + warp * (kTokGroup * kChunkCols);
+  float* act = s.act + warp * (kTG * kCC);
+  uint32_t lb[R];
+#pragma unroll
+  for (int g = 0; g < R; ++g) lb[g] = (static_cast<uint32_t>(g) << 7) | (lane << 2);
 #pragma unroll
   for (int g = 0; g < R; ++g)
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[g][t] = 0.f;
-  for (int kw0 = kw_lo; kw0 < kw_hi; kw0 += kChunkWords) {
-    const int nw = min(kChunkWords, kw_hi - kw0);
+  if (kw_lo >= kw_hi) return;
+  uint32_t nxt[R][Q];
+#pragma unroll
+  for (int g = 0; g < R; ++g)
+#pragma unroll
+    for (int p = 0; p < Q; ++p)
+      nxt[g][p] = __ldg(planes + p * plane_stride + static_cast<long long>(kw_lo) * N + row[g]);
+  for (int kw0 = kw_lo; kw0 < kw_hi; kw0 += kCW) {
+    const int nw = min(kCW, kw_hi - kw0);
     __syncwarp();
     load_chunk(act, kw0 * 32, nw * 32);
     __syncwarp();
     for (int ww = 0; ww < nw; ++ww) {
-      uint32_t pl[R][Q];
+      uint32_t cur[R][Q];
 #pragma unroll
       for (int g = 0; g < R; ++g)
 #pragma unroll
-        for (int p = 0; p < Q; ++p)
-          pl[g][p] = __ldg(planes + p * plane_stride + static_cast<long long>(row[g]) * KW + kw0 + ww);
-      const float* a_col = act + ww * 32;
-#pragma unroll 4
-      for (int t = 0; t < 32; ++t) {
-        float w[R];
+        for (int p = 0; p < Q; ++p) cur[g][p] = nxt[g][p];
+      const int kn = kw0 + ww + 1;
+      if (kn < kw_hi) {
 #pragma unroll
-        for (int g = 0; g < R; ++g) {
-          uint32_t idx = 0;
+        for (int g = 0; g < R; ++g)
 #pragma unroll
-          for (int p = 0; p < Q; ++p) idx = (idx << 1) | ((pl[g][p] >> t) & 1u);
-          w[g] = s.lut[(g * (1 << Q) + idx) * 32 + lane];
-        }
+          for (int p = 0; p < Q; ++p)
+            nxt[g][p] = __ldg(planes + p * plane_stride + static_cast<long long>(kn) * N + row[g]);
+      }
+      uint32_t ib[R][8];
 #pragma unroll
-        for (int tk = 0; tk < NT; ++tk) {
-          const float x = a_col[tk * kChunkCols + t];
+      for (int g = 0; g < R; ++g) planes_to_index_bytes<Q>(cur[g], ib[g]);
+      const float* xa = act + ww * 32;
 #pragma unroll
-          for (int g = 0; g < R; ++g) acc[g][tk] = fmaf(x, w[g], acc[g][tk]);
+      for (int m = 0; m < 8; ++m) {
+        float4 xv[NT];
+#pragma unroll
+        for (int tk = 0; tk < NT; ++tk)
+          xv[tk] = *reinterpret_cast<const float4*>(xa + tk * kCC + 4 * m);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int g = 0; g < R; ++g) {
+            const uint32_t off = __byte_perm(ib[g][m], lb[g], 0x6504 | (j << 4));
+            const float w = *reinterpret_cast<const float*>(s.lut + off);
+#pragma unroll
+            for (int tk = 0; tk < NT; ++tk) acc[g][tk] = fmaf(lane4(xv[tk], j), w, acc[g][tk]);
+          }
         }
       }
     }
@@ -229,46 +305,43 @@ __device__ void gateup_group(const LayerArgs& a, const Route& r, const pw_block_
                              int i0, int g0, int nt, const SmemPtrs& s, float* h_ws) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int KW = a.H / 32;
-  const long long plane_stride = static_cast<long long>(2 * a.I) * KW;
+  const int N = 2 * a.I;
+  const long long plane_stride = static_cast<long long>(N) * KW;
   const int row[2] = {i0 + lane, a.I + i0 + lane};
   int lo, hi;
   warp_range(KW, lo, hi);
+  int tok[NT];
+#pragma unroll
+  for (int tk = 0; tk < NT; ++tk) tok[tk] = (tk < nt) ? s.pairs[g0 + tk] / a.k : -1;
   auto loader = [&](float* act, int c0, int cols) {
+    const int c = lane * 4;
+#pragma unroll
     for (int tk = 0; tk < NT; ++tk) {
-      const bool live = tk < nt;
-      const int t = live ? s.pairs[g0 + tk] / a.k : 0;
-      const uint16_t* src = a.hidden + static_cast<long long>(t) * a.H + c0;
-      for (int c = lane * 8; c < cols; c += 256) {
-        float v[8];
-        if (live) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(src + c);
-          const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = bf16_bits_to_float(h[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = 0.f;
-        }
-        float4* d = reinterpret_cast<float4*>(act + tk * kChunkCols + c);
-        d[0] = make_float4(v[0], v[1], v[2], v[3]);
-        d[1] = make_float4(v[4], v[5], v[6], v[7]);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (tok[tk] >= 0 && c < cols) {
+        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(
+            a.hidden + static_cast<long long>(tok[tk]) * a.H + c0 + c));
+        v = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                        __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
       }
+      *reinterpret_cast<float4*>(act + tk * kCC + c) = v;
     }
   };
   float acc[2][NT];
-  rows_dot<Q, 2, NT>(ent.planes, plane_stride, row, lo, hi, KW, s, loader, acc);
+  rows_dot<Q, 2, NT>(ent.planes, plane_stride, N, row, lo, hi, s, loader, acc);
 #pragma unroll
   for (int tk = 0; tk < NT; ++tk) {
-    s.red[((warp * kTokGroup + tk) * 2 + 0) * 32 + lane] = acc[0][tk];
-    s.red[((warp * kTokGroup + tk) * 2 + 1) * 32 + lane] = acc[1][tk];
+    s.red[((warp * kTG + tk) * 2 + 0) * 32 + lane] = acc[0][tk];
+    s.red[((warp * kTG + tk) * 2 + 1) * 32 + lane] = acc[1][tk];
   }
   __syncthreads();
   if (threadIdx.x < 32 * nt) {
     const int tk = threadIdx.x >> 5;
     float g = 0.f, u = 0.f;
+#pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      g += s.red[((w * kTokGroup + tk) * 2 + 0) * 32 + lane];
-      u += s.red[((w * kTokGroup + tk) * 2 + 1) * 32 + lane];
+      g += s.red[((w * kTG + tk) * 2 + 0) * 32 + lane];
+      u += s.red[((w * kTG + tk) * 2 + 1) * 32 + lane];
     }
     const float h = g / (1.f + expf(-g)) * u;
     h_ws[static_cast<long long>(r.off + g0 + tk) * a.I + i0 + lane] = h;
@@ -282,16 +355,15 @@ __device__ void gateup_tile(const LayerArgs& a, const Route& r, const pw_block_e
   const int row0[2] = {i0, a.I + i0};
   load_luts<Q, 2>(ent.lut, row0, s);
   __syncthreads();
-  for (int g0 = 0; g0 < r.ne; g0 += kTokGroup) {
-    const int nt = min(kTokGroup, r.ne - g0);
+  for (int g0 = 0; g0 < r.ne; g0 += kTG) {
+    const int nt = min(kTG, r.ne - g0);
     if (nt == 1) gateup_group<Q, 1>(a, r, ent, i0, g0, nt, s, h_ws);
     else if (nt == 2) gateup_group<Q, 2>(a, r, ent, i0, g0, nt, s, h_ws);
-    else if (nt <= 4) gateup_group<Q, 4>(a, r, ent, i0, g0, nt, s, h_ws);
-    else gateup_group<Q, 8>(a, r, ent, i0, g0, nt, s, h_ws);
+    else gateup_group<Q, 4>(a, r, ent, i0, g0, nt, s, h_ws);
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(const LayerArgs a, float* h_ws,
+__global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerArgs a, float* h_ws,
                                                                     int* tile_count) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const SmemPtrs s = carve(smem_raw);
@@ -303,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(const LayerA
     const long long cta = blockIdx.y * static_cast<long long>(gridDim.x) + blockIdx.x;
     const long long stride = static_cast<long long>(gridDim.x) * gridDim.y * kThreads;
     for (long long i = cta * kThreads + threadIdx.x; i < total; i += stride) a.out[i] = 0.f;
-    for (long long i = cta * kThreads + threadIdx.x; i < a.H / kRows; i += stride) tile_count[i] = 0;
+    const int n_tiles = (a.H + kDownRows - 1) / kDownRows;
+    for (long long i = cta * kThreads + threadIdx.x; i < n_tiles; i += stride) tile_count[i] = 0;
   }
   const bool report = blockIdx.x == 0;
   const Route r = route_slot(a, blockIdx.y, s, report);
@@ -313,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(const LayerA
     if (report) latch_status(a.status, PW_ERR_PAGE_NOT_RESIDENT);
     return;
   }
-  const int i0 = blockIdx.x * kRows;
+  const int i0 = blockIdx.x * kPairsPerTile;
   switch (ent.q) {
     case 3: gateup_tile<3>(a, r, ent, i0, s, h_ws); break;
     case 4: gateup_tile<4>(a, r, ent, i0, s, h_ws); break;
@@ -327,69 +400,83 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(const LayerA
 
 // ---------------------------------------------------------------- down
 
-template <int Q, int NT>
+template <int Q, int R, int NT>
 __device__ void down_group(const LayerArgs& a, const Route& r, const pw_block_entry& ent,
                            int n0, int g0, int nt, const SmemPtrs& s, const float* h_ws,
                            float* y_ws) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int KW = a.I / 32;
-  const long long plane_stride = static_cast<long long>(a.H) * KW;
-  const int row[1] = {n0 + lane};
+  const int N = a.H;
+  const long long plane_stride = static_cast<long long>(N) * KW;
+  int row[R];
+#pragma unroll
+  for (int g = 0; g < R; ++g) row[g] = n0 + 32 * g + lane;
   int lo, hi;
   warp_range(KW, lo, hi);
   auto loader = [&](float* act, int c0, int cols) {
+    const int c = lane * 4;
+#pragma unroll
     for (int tk = 0; tk < NT; ++tk) {
-      const bool live = tk < nt;
-      const float* src = h_ws + static_cast<long long>(r.off + g0 + (live ? tk : 0)) * a.I + c0;
-      for (int c = lane * 8; c < cols; c += 256) {
-        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
-        if (live) {
-          v0 = *reinterpret_cast<const float4*>(src + c);
-          v1 = *reinterpret_cast<const float4*>(src + c + 4);
-        }
-        float4* d = reinterpret_cast<float4*>(act + tk * kChunkCols + c);
-        d[0] = v0;
-        d[1] = v1;
-      }
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (tk < nt && c < cols)
+        v = *reinterpret_cast<const float4*>(h_ws + static_cast<long long>(r.off + g0 + tk) * a.I +
+                                             c0 + c);
+      *reinterpret_cast<float4*>(act + tk * kCC + c) = v;
     }
   };
-  float acc[1][NT];
-  rows_dot<Q, 1, NT>(ent.planes, plane_stride, row, lo, hi, KW, s, loader, acc);
+  float acc[R][NT];
+  rows_dot<Q, R, NT>(ent.planes, plane_stride, N, row, lo, hi, s, loader, acc);
 #pragma unroll
-  for (int tk = 0; tk < NT; ++tk) s.red[((warp * kTokGroup + tk) * 2) * 32 + lane] = acc[0][tk];
+  for (int tk = 0; tk < NT; ++tk)
+#pragma unroll
+    for (int g = 0; g < R; ++g) s.red[((warp * kTG + tk) * 2 + g) * 32 + lane] = acc[g][tk];
   __syncthreads();
-  if (threadIdx.x < 32 * nt) {
-    const int tk = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 32 * R * nt; i += kThreads) {
+    const int L = i & 31, g = (i >> 5) % R, tk = (i >> 5) / R;
     float y = 0.f;
-    for (int w = 0; w < kWarps; ++w) y += s.red[((w * kTokGroup + tk) * 2) * 32 + lane];
-    y_ws[static_cast<long long>(s.pairs[g0 + tk]) * a.H + n0 + lane] = y;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) y += s.red[((w * kTG + tk) * 2 + g) * 32 + L];
+    y_ws[static_cast<long long>(s.pairs[g0 + tk]) * a.H + n0 + 32 * g + L] = y;
   }
   __syncthreads();
 }
 
-template <int Q>
+template <int Q, int R>
 __device__ void down_tile(const LayerArgs& a, const Route& r, const pw_block_entry& ent, int n0,
                           const SmemPtrs& s, const float* h_ws, float* y_ws) {
-  const int row0[1] = {n0};
-  load_luts<Q, 1>(ent.lut, row0, s);
+  int row0[R];
+#pragma unroll
+  for (int g = 0; g < R; ++g) row0[g] = n0 + 32 * g;
+  load_luts<Q, R>(ent.lut, row0, s);
   __syncthreads();
-  for (int g0 = 0; g0 < r.ne; g0 += kTokGroup) {
-    const int nt = min(kTokGroup, r.ne - g0);
-    if (nt == 1) down_group<Q, 1>(a, r, ent, n0, g0, nt, s, h_ws, y_ws);
-    else if (nt == 2) down_group<Q, 2>(a, r, ent, n0, g0, nt, s, h_ws, y_ws);
-    else if (nt <= 4) down_group<Q, 4>(a, r, ent, n0, g0, nt, s, h_ws, y_ws);
-    else down_group<Q, 8>(a, r, ent, n0, g0, nt, s, h_ws, y_ws);
+  for (int g0 = 0; g0 < r.ne; g0 += kTG) {
+    const int nt = min(kTG, r.ne - g0);
+    if (nt == 1) down_group<Q, R, 1>(a, r, ent, n0, g0, nt, s, h_ws, y_ws);
+    else if (nt == 2) down_group<Q, R, 2>(a, r, ent, n0, g0, nt, s, h_ws, y_ws);
+    else down_group<Q, R, 4>(a, r, ent, n0, g0, nt, s, h_ws, y_ws);
+  }
+}
+
+template <int R>
+__device__ void down_dispatch(const LayerArgs& a, const Route& r, const pw_block_entry& ent,
+                              int n0, const SmemPtrs& s, const float* h_ws, float* y_ws) {
+  switch (ent.q) {
+    case 3: down_tile<3, R>(a, r, ent, n0, s, h_ws, y_ws); break;
+    case 4: down_tile<4, R>(a, r, ent, n0, s, h_ws, y_ws); break;
+    case 5: down_tile<5, R>(a, r, ent, n0, s, h_ws, y_ws); break;
+    case 6: down_tile<6, R>(a, r, ent, n0, s, h_ws, y_ws); break;
+    default: down_tile<8, R>(a, r, ent, n0, s, h_ws, y_ws); break;
   }
 }
 
 // Pairs of an expert that cannot be computed contribute zero.
-__device__ void zero_pairs(const LayerArgs& a, const Route& r, int n0, const SmemPtrs& s,
-                           float* y_ws) {
-  for (int i = threadIdx.x; i < r.ne * 32; i += kThreads)
-    y_ws[static_cast<long long>(s.pairs[i >> 5]) * a.H + n0 + (i & 31)] = 0.f;
+__device__ void zero_pairs(const LayerArgs& a, const Route& r, int n0, int rows,
+                           const SmemPtrs& s, float* y_ws) {
+  for (int i = threadIdx.x; i < r.ne * rows; i += kThreads)
+    y_ws[static_cast<long long>(s.pairs[i / rows]) * a.H + n0 + (i % rows)] = 0.f;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(const LayerArgs a, const float* h_ws,
+__global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArgs a, const float* h_ws,
                                                                   float* y_ws, int* tile_count) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const SmemPtrs s = carve(smem_raw);
@@ -398,23 +485,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(const LayerArg
   const pw_block_entry gu = a.table[2 * r.e];
   const pw_block_entry ent = a.table[2 * r.e + 1];
   const bool report = blockIdx.x == 0;
-  const int n0 = blockIdx.x * kRows;
+  const int n0 = blockIdx.x * kDownRows;
+  const int rows = min(kDownRows, a.H - n0);   // 64, or 32 on a ragged last tile
   if (gu.state != PW_PAGE_GPU || ent.state != PW_PAGE_GPU) {
     if (report) latch_status(a.status, PW_ERR_PAGE_NOT_RESIDENT);
-    zero_pairs(a, r, n0, s, y_ws);
-  } else if (!supported_q(gu.q)) {
-    zero_pairs(a, r, n0, s, y_ws);  // gate_up skipped this expert; h is not valid
+    zero_pairs(a, r, n0, rows, s, y_ws);
+  } else if (!supported_q(gu.q) || !supported_q(ent.q)) {
+    if (report && !supported_q(ent.q)) latch_status(a.status, PW_ERR_UNSUPPORTED_Q);
+    zero_pairs(a, r, n0, rows, s, y_ws);  // an unusable block: this expert contributes 0
+  } else if (rows == kDownRows) {
+    down_dispatch<2>(a, r, ent, n0, s, h_ws, y_ws);
   } else {
-    switch (ent.q) {
-      case 3: down_tile<3>(a, r, ent, n0, s, h_ws, y_ws); break;
-      case 4: down_tile<4>(a, r, ent, n0, s, h_ws, y_ws); break;
-      case 5: down_tile<5>(a, r, ent, n0, s, h_ws, y_ws); break;
-      case 6: down_tile<6>(a, r, ent, n0, s, h_ws, y_ws); break;
-      case 8: down_tile<8>(a, r, ent, n0, s, h_ws, y_ws); break;
-      default:
-        if (report) latch_status(a.status, PW_ERR_UNSUPPORTED_Q);
-        zero_pairs(a, r, n0, s, y_ws);
-    }
+    down_dispatch<1>(a, r, ent, n0, s, h_ws, y_ws);
   }
   // Arrival: the last of the routed experts' CTAs on this row tile combines.
   __threadfence();
@@ -428,16 +510,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(const LayerArg
   __syncthreads();
   if (!s.misc[4]) return;
   __threadfence();
-  const int lane = threadIdx.x & 31;
-  for (int t = threadIdx.x >> 5; t < a.T; t += kWarps) {
+  for (int i = threadIdx.x; i < a.T * rows; i += kThreads) {
+    const int t = i / rows, n = n0 + i % rows;
     float acc = 0.f;
     for (int j = 0; j < a.k; ++j) {
       const int p = t * a.k + j;
       const int e = a.topk_ids[p];
       if (e < 0 || e >= a.E) continue;
-      acc = fmaf(a.topk_weights[p], __ldcg(y_ws + static_cast<long long>(p) * a.H + n0 + lane), acc);
+      acc = fmaf(a.topk_weights[p], __ldcg(y_ws + static_cast<long long>(p) * a.H + n), acc);
     }
-    a.out[static_cast<long long>(t) * a.H + n0 + lane] = acc;
+    a.out[static_cast<long long>(t) * a.H + n] = acc;
   }
 }
 
@@ -454,7 +536,7 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 size_t decode_workspace_bytes(const pw_moe_shape& s) {
   const size_t pairs = static_cast<size_t>(s.T) * s.k;
   return round256(sizeof(float) * pairs * s.I) + round256(sizeof(float) * pairs * s.H) +
-         round256(sizeof(int) * (s.H / kRows));
+         round256(sizeof(int) * (s.H / 32));
 }
 
 cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream) {
@@ -478,12 +560,12 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream) {
   float* y_ws = reinterpret_cast<float*>(base);
   base += round256(sizeof(float) * static_cast<size_t>(n_pairs) * a.H);
   int* tile_count = reinterpret_cast<int*>(base);
-  decode_gateup_kernel<<<dim3(a.I / kRows, slots), kThreads, kSmemBytes, stream>>>(a, h_ws,
-                                                                                   tile_count);
+  decode_gateup_kernel<<<dim3(a.I / kPairsPerTile, slots), kThreads, kSmemBytes, stream>>>(
+      a, h_ws, tile_count);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_down_kernel<<<dim3(a.H / kRows, slots), kThreads, kSmemBytes, stream>>>(a, h_ws, y_ws,
-                                                                                 tile_count);
+  decode_down_kernel<<<dim3((a.H + kDownRows - 1) / kDownRows, slots), kThreads, kSmemBytes,
+                       stream>>>(a, h_ws, y_ws, tile_count);
   return cudaGetLastError();
 }
 

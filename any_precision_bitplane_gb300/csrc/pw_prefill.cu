@@ -16,7 +16,8 @@
 //
 // GEMM kernel (one CTA per SM, persistent over a static tile list):
 //   warps 0-3  dequant producers, thread r owns A-tile row r: read the row's
-//              top-q plane words, rebuild each index, look it up in the row's
+//              top-q plane words (one word column of 128 consecutive rows is
+//              contiguous, so these loads coalesce), rebuild each index, look it up in the row's
 //              LUT (shared memory) and write fp16 into the 128-byte-swizzled,
 //              K-major A stage; then the epilogue of the same rows from TMEM.
 //   warp 4     TMA producer for the token operand (fp16 rows, 128B swizzle).
@@ -257,14 +258,13 @@ __device__ void report_unusable(Mode mode, const GemmArgs& a, int e) {
 // Thread r: fill A-stage row r with the 64 weights of k-step s.
 template <int Q>
 __device__ __forceinline__ void dequant_kstep(const uint32_t* row_planes, long long plane_stride,
-                                              int s, const uint16_t* lut_s, int r,
+                                              long long N, int s, const uint16_t* lut_s, int r,
                                               uint8_t* a_stage) {
   uint32_t w[Q][2];
 #pragma unroll
   for (int p = 0; p < Q; ++p) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2*>(row_planes + p * plane_stride + s * 2));
-    w[p][0] = v.x;
-    w[p][1] = v.y;
+    w[p][0] = __ldg(row_planes + p * plane_stride + (2 * s) * N);
+    w[p][1] = __ldg(row_planes + p * plane_stride + (2 * s + 1) * N);
   }
   const uint32_t row_base = (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
@@ -315,13 +315,13 @@ __device__ void dequant_tile(const GemmArgs& a, Mode mode, const pw_block_entry&
   const int KW = K / 32;
   const long long N = (mode == kGateUp) ? 2LL * a.I : a.H;
   const long long plane_stride = N * KW;
-  const uint32_t* row_planes = ent.planes + static_cast<long long>(grow) * KW;
+  const uint32_t* row_planes = ent.planes + grow;
   for (int s = 0; s < ksteps; ++s, ++it) {
     const int stage = it % NST;
     const uint32_t par = (it / NST) & 1u;
     if (*abort) continue;
     if (!mbar_wait(bar_base + 8 * (kBarEmpty + stage), par ^ 1u, abort, a.status)) continue;
-    dequant_kstep<Q>(row_planes, plane_stride, s, lut_s, r, smem + kOffA + stage * kAStage);
+    dequant_kstep<Q>(row_planes, plane_stride, N, s, lut_s, r, smem + kOffA + stage * kAStage);
     fence_proxy_async();
     mbar_arrive(bar_base + 8 * (kBarFullA + stage));
   }

@@ -5,8 +5,8 @@ overlay bitplane format with the library's own packing kernel, and builds the
 page table (PagedWeight, "Core components" 1: one entry per linear block with
 its committed bitwidth).  Memory layout in HBM, per layer:
 
-  planes_gu  int32 [E, 8, 2I, H/32]   (raw uint32 plane words, plane-major per block)
-  planes_dn  int32 [E, 8, H, I/32]
+  planes_gu  int32 [E, 8, H/32, 2I]   (raw uint32 plane words: plane, word, row)
+  planes_dn  int32 [E, 8, I/32, H]
   lut_gu[b]  fp16  [E, 2I, 2^b]       for b in 3, 4, 5, 6, 8
   lut_dn[b]  fp16  [E, H, 2^b]
 
@@ -26,8 +26,8 @@ class DeviceLayer:
         self.E, self.H, self.I, self.k = cfg.E, cfg.H, cfg.I, cfg.k
         self.device = torch.device(device)
         E, H, I = self.E, self.H, self.I
-        self.planes_gu = torch.empty((E, 8, 2 * I, H // 32), dtype=torch.int32, device=device)
-        self.planes_dn = torch.empty((E, 8, H, I // 32), dtype=torch.int32, device=device)
+        self.planes_gu = torch.empty((E, 8, H // 32, 2 * I), dtype=torch.int32, device=device)
+        self.planes_dn = torch.empty((E, 8, I // 32, H), dtype=torch.int32, device=device)
         for e in range(E):
             codes = torch.from_numpy(np.ascontiguousarray(layer.codes_gu[e])).to(device)
             pack_bitplanes(codes, planes=self.planes_gu[e])

@@ -48,6 +48,9 @@ def parse_args():
     ap.add_argument("--T", type=int, default=4, help="tokens per step (decode batch)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the other batch sizes")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="layer copies to rotate (0: enough to exceed 2x L2)")
     return ap.parse_args()
 
 
@@ -165,7 +168,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- native arm
 
-def setup_workload(name, T, device):
+def setup_workload(name, T, device, copies=0):
     import torch
     import any_precision_bitplane_gb300 as pw
     from any_precision_bitplane_gb300.layer import DeviceLayer
@@ -182,7 +185,8 @@ def setup_workload(name, T, device):
     ids_host = ids.cpu().numpy()
     weight_bytes = base.routed_bytes(ids_host)
     step_bytes = weight_bytes + T * cfg.H * 2 + T * cfg.k * 8 + T * cfg.H * 4
-    copies = max(2, math.ceil(2 * L2_BYTES / max(weight_bytes, 1)))
+    if copies <= 0:
+        copies = max(2, math.ceil(2 * L2_BYTES / max(weight_bytes, 1)))
     layers = [base] + [base.clone() for _ in range(copies - 1)]
     host = {"hidden": tok.hidden_bf16.view(np.int16), "ids": ids_host,
             "wts": wts.cpu().numpy()}
@@ -343,7 +347,7 @@ def native(args):
     peak, peak_kind = measured_peaks()
 
     cfg, layer, layers, hidden, ids, wts, step_bytes, weight_bytes, host = \
-        setup_workload(args.workload, args.T, device)
+        setup_workload(args.workload, args.T, device, args.copies)
     stream = torch.cuda.Stream(device)
     g, start, stop, out = time_device(pw, cfg, layers, hidden, ids, wts, args.steps,
                                       args.warmup, stream)
@@ -375,8 +379,11 @@ def native(args):
     per_launch_s = ms / 1e3 / args.steps
     achieved = step_bytes / per_launch_s / 1e9
 
-    e2e_dt, bi, bo = time_e2e(pw, cfg, layers, host, args.steps, args.warmup, device)
-    e2e_value = T * args.steps * world / e2e_dt
+    e2e = None
+    if not args.no_e2e:
+        e2e_dt, bi, bo = time_e2e(pw, cfg, layers, host, args.steps, args.warmup, device)
+        e2e = {"value": T * args.steps * world / e2e_dt, "unit": "tokens/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
 
     sweep = {}
     if not args.no_sweep and rank == 0 and world == 1:
@@ -432,8 +439,7 @@ def native(args):
                      "kernel": "pw_moe_forward decode launch pair (gateup + down)",
                      "bytes_per_launch": step_bytes,
                      "traffic": recorded_traffic(args.workload, T)},
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo},
+        "e2e": e2e,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }

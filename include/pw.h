@@ -15,10 +15,12 @@
  *
  * Storage format (the pages give none; this is the library's contract):
  *   - A block with N rows and K columns (K % 32 == 0) stores 8 bitplanes of
- *     its 8-bit codes, uint32 [8][N][K/32], plane-major.  Plane p holds bit
+ *     its 8-bit codes, uint32 [8][K/32][N], plane-major.  Plane p holds bit
  *     (7 - p) of every code (plane 0 = most significant), so the top q planes
- *     are the first q planes, a contiguous prefix.  Within a plane, row n's
- *     word w holds columns 32w..32w+31, column 32w+t at bit t.
+ *     are the first q planes, a contiguous prefix.  Within a plane, word w of
+ *     row n (at [p][w][n]) holds columns 32w..32w+31 of row n, column 32w+t
+ *     at bit t; the N words of a word column are contiguous, so 32
+ *     consecutive rows' words are 128 contiguous bytes.
  *   - Reading q planes gives idx_q = code >> (8 - q).  Row n's q-bit LUT holds
  *     2^q fp16 values, fp16 [N][2^q]; the weight is LUT_q[n][idx_q].
  *   - Expert e owns block 2e (gate_up, N = 2I rows x K = H: rows 0..I-1 gate,
@@ -79,7 +81,7 @@ extern "C" {
 typedef struct pw_block_entry {
   int32_t q;               /* committed bitwidth q_i, in {3,4,5,6,8}                   */
   int32_t state;           /* PW_PAGE_*                                                */
-  const uint32_t* planes;  /* device: uint32 [>= q][N][K/32], the block's planes      */
+  const uint32_t* planes;  /* device: uint32 [>= q][K/32][N], the block's planes      */
   const uint16_t* lut;     /* device: fp16 [N][2^q], the LUT for the committed q       */
 } pw_block_entry;
 
@@ -107,7 +109,7 @@ int pw_version(void);
  * Encode 8-bit codes into the overlay bitplane format (PagedWeight, "Core
  * components" 1, APL overlay bitplanes).
  *   codes  device uint8 [N][K], row-major
- *   planes device uint32 [8][N][K/32] (output)
+ *   planes device uint32 [8][K/32][N] (output)
  * Errors: PW_ERR_INVALID_ARG (null, N < 0), PW_ERR_SHAPE (K % 32 != 0 or
  * K <= 0). */
 int pw_pack_bitplanes(const uint8_t* codes, int32_t N, int32_t K,
@@ -116,7 +118,7 @@ int pw_pack_bitplanes(const uint8_t* codes, int32_t N, int32_t K,
 /* Read a block's top b planes back into b-bit indices, idx = code >> (8-b)
  * (PagedWeight, "Core components" 1: a b-bit view reads the top b planes).
  * Exposed so that the bit extraction can be checked bit-exactly.
- *   planes device uint32 [>= b][N][K/32];  idx device uint8 [N][K] (output)
+ *   planes device uint32 [>= b][K/32][N];  idx device uint8 [N][K] (output)
  * Errors: PW_ERR_INVALID_ARG, PW_ERR_SHAPE, PW_ERR_UNSUPPORTED_Q (b not in 1..8). */
 int pw_unpack_top(const uint32_t* planes, int32_t N, int32_t K, int32_t b,
                   uint8_t* idx, cudaStream_t stream);

@@ -87,7 +87,7 @@ def expert_outputs(hidden_bf16: np.ndarray, topk_ids: np.ndarray, block: BlockFn
                    tokens: Optional[Sequence[int]] = None) -> Dict[int, np.ndarray]:
     """y_e(x_t) (fp64 [H]) for every routed pair p = t*k + j, keyed by p.
 
-    block(e, m) returns (planes uint32 [8, N, K/32], lut_q fp16 [N, 2^q], q)
+    block(e, m) returns (planes uint32 [8, K/32, N], lut_q fp16 [N, 2^q], q)
     for block 2e+m (m = 0 gate_up, m = 1 down), as the page table commits it.
     `experts` / `tokens` restrict the pairs computed (default: all).
     """

@@ -51,13 +51,14 @@ def test_pack_full_size_block_sampled_rows(pw):
     codes = rng.integers(0, 256, size=(N, K), dtype=np.uint8)
     planes = _u32(pw.pack_bitplanes(torch.from_numpy(codes).cuda()))
     rows = np.concatenate([[0, 1, N - 1], rng.choice(N, 61, replace=False)])
-    np.testing.assert_array_equal(planes[:, rows], apl.pack_bitplanes(codes[rows]))
+    np.testing.assert_array_equal(planes[:, :, rows], apl.pack_bitplanes(codes[rows]))
 
 
 def test_pack_worked_example_on_gpu(pw):
     codes = np.zeros((2, 64), np.uint8)
     codes[0, 0], codes[0, 33], codes[1, 31], codes[1, 40] = 176, 1, 255, 66
     planes = _u32(pw.pack_bitplanes(torch.from_numpy(codes).cuda()))
+    # planes[p, w, n]: word w of row n
     assert planes[0, 0, 0] == 1 and planes[2, 0, 0] == 1 and planes[3, 0, 0] == 1
-    assert planes[7, 0, 1] == 2 and planes[1, 1, 1] == 0x100 and planes[6, 1, 1] == 0x100
-    assert all(planes[p, 1, 0] == 0x80000000 for p in range(8))
+    assert planes[7, 1, 0] == 2 and planes[1, 1, 1] == 0x100 and planes[6, 1, 1] == 0x100
+    assert all(planes[p, 0, 1] == 0x80000000 for p in range(8))

@@ -31,12 +31,12 @@ def _read_golden(name):
 def test_pack_worked_example():
     rows = _read_golden("bitplane_worked_example.txt")
     codes = np.zeros((2, 64), np.uint8)
-    want = np.zeros((8, 2, 2), np.uint32)
+    want = np.zeros((8, 2, 2), np.uint32)            # [plane][word][row]
     for r in rows:
         if r[0] == "code":
             codes[int(r[1]), int(r[2])] = int(r[3])
         elif r[0] == "plane":
-            want[int(r[1]), int(r[2]), int(r[3])] = int(r[4], 16)
+            want[int(r[1]), int(r[3]), int(r[2])] = int(r[4], 16)
     got = apl.pack_bitplanes(codes)
     np.testing.assert_array_equal(got, want)
     for r in rows:
