@@ -1,32 +1,36 @@
 // Fused mixed-precision MoE layer, decode path (few tokens per expert).
 //
-// PagedWeight, "Core components" 3 (fused mixed-precision kernel): the kernel
-// reads every linear block's bitplanes and LUT directly, each block at its own
-// committed bitwidth q_i, inside one fused operation.  Two launches:
+// PagedWeight, "Core components" 3 (fused mixed-precision kernel): every
+// linear block's bitplanes and LUT are read directly, each block at its own
+// committed bitwidth q_i, inside one fused operation.  Three launches, chained
+// with programmatic dependent launch so that each one's start-up overlaps the
+// previous one's tail:
 //
-//   gateup: per (routed expert e, tile of 32 gate/up row pairs): read the top
-//           q planes of gate rows i and up rows I+i, rebuild the q-bit codes,
-//           look them up in each row's LUT, dot with the expert's gathered
-//           hidden rows (fp32), then h = SiLU(g) * u -> workspace.
-//   down:   per (routed expert e, tile of 64 down rows): same bitplane/LUT
-//           read at the down block's q, dot with h -> y for each of e's pairs
-//           (workspace).  The last CTA to finish a row tile (a per-tile
-//           arrival counter) combines out[t] = sum_j w_tj * y[t*k + j] over
-//           the tile in j order, so the output is deterministic.
+//   prep:    CTA 0 groups the (token, expert) pairs by expert (stable), lists
+//            the routed experts largest-bitwidth first (so the costliest
+//            tiles are scheduled first), and resets the tile counters; the
+//            other CTAs widen the hidden states to fp32 and zero `out`.
+//   gate_up: persistent CTAs take tiles (routed expert, 32 gate/up row pairs)
+//            from an atomic counter: read the top q planes of gate rows i and
+//            up rows I+i, rebuild the q-bit codes, look them up in each row's
+//            LUT, dot with the expert's tokens (fp32), h = SiLU(g) * u.
+//   down:    persistent CTAs take tiles (routed expert, 64 down rows): same
+//            read of the down block, dot with h -> y for each pair.  The last
+//            tile to finish a 64-row range (arrival counter) forms
+//            out[t] = sum_j w_tj * y[t*k + j] over the range in j order, so
+//            the output is deterministic.
 //
-// Work inside a CTA: lane L owns rows (row0 + L) and (row0' + L) of the tile;
-// the 8 warps split the K columns and their partial sums meet in shared
-// memory.  Per 32 columns a lane loads one word of each of the top q planes
-// per row (a word column of consecutive rows is contiguous, so a warp's load
-// is one 128-byte line), turns the q words into 32 index bytes with a byte
-// transpose and an 8x8 bit-matrix transpose, and looks each index up in its
-// row's LUT, which sits in a lane-private shared-memory column: one byte
-// permute forms the address (index * 256 + slot * 128 + lane * 4), and every
-// lookup of lane L hits bank L.
-//
-// Each CTA finds its expert itself from topk_ids (count, pick the slot-th
-// routed expert, list its pairs in ascending pair order), so no separate
-// routing launch is needed on this path.
+// Work inside a CTA: each lane owns one or two rows of the tile; the 8 warps
+// split the K columns and their partial sums meet in shared memory.  A warp
+// streams its word columns through a 3-stage cp.async ring: per column, one
+// word of each of the top q planes per row (a word column of consecutive
+// rows is contiguous, so each copy is part of a 128-byte line) plus the 32
+// matching activations of up to 4 tokens.  A lane turns its q words into 32
+// index bytes with a byte transpose and an 8x8 bit-matrix transpose and
+// looks each index up in its row's LUT, held in a lane-private
+// shared-memory column (every lookup of lane L hits bank L); a byte permute
+// of the index byte forms the offset.  Products accumulate as packed fp32
+// pairs.  q = 8 blocks stream one row per lane so that their LUTs fit.
 #include <cuda_fp16.h>
 
 #include "pw_internal.cuh"
@@ -40,125 +44,128 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kPairsPerTile = 32;   // gate_up tile: 32 gate rows + their 32 up rows
 constexpr int kDownRows = 64;       // down tile: two 32-row groups
 constexpr int kTG = 4;              // tokens per pass over the weights
-constexpr int kCW = 4;              // words per staged activation chunk
-constexpr int kCC = kCW * 32;       // columns per staged activation chunk
+constexpr int kStages = 3;          // per-warp cp.async ring depth (word columns)
 constexpr int kMaxPairs = 4096;     // T*k limit of this path
 constexpr int kMaxExperts = 1024;
+constexpr int kPrepThreads = 256;
+constexpr int kPrepWarps = kPrepThreads / 32;
 
-// Shared memory (bytes).  The LUT region comes first: entry v of row slot g
-// for lane L sits at byte v*256 + g*128 + L*4 (fp32), so a lane's lookups
-// always hit bank L and one byte permute turns an 8-bit index into the offset.
-constexpr int kLutBytes = 256 * 256;
-constexpr int kActBytes = kWarps * kTG * kCC * 4;
+// One ring stage holds one word column (32 weights) of every streamed row:
+// q*R plane words per lane (at most 12: q <= 6 with two row slots, or q = 8
+// with one) and the matching 32 activations of up to kTG tokens.
+constexpr int kStagePlaneBytes = 12 * 128;
+constexpr int kStageBytes = kStagePlaneBytes + kTG * 128;
+
+// Shared memory (bytes).  LUT region first.  Two layouts:
+//   paired  (q <= 6, two row slots): entry v of slot g for lane L at
+//           v*256 + g*128 + L*4, so one byte permute of the index byte forms
+//           the offset;
+//   compact (q = 8, one row slot):   entry v for lane L at v*128 + L*4 (the
+//           permute gives v*256 + L*8, halved by one shift).
+// Either way a lane's lookups always hit bank L.
+constexpr int kLutBytes = 32768;
+constexpr int kRingBytes = kWarps * kStages * kStageBytes;
 constexpr int kRedBytes = kWarps * kTG * 2 * 32 * 4;
-constexpr int kCountBytes = kMaxExperts * 4;
-constexpr int kPairBytes = kMaxPairs * 4;
-constexpr int kOffAct = kLutBytes;
-constexpr int kOffRed = kOffAct + kActBytes;
-constexpr int kOffCount = kOffRed + kRedBytes;
-constexpr int kOffPairs = kOffCount + kCountBytes;
-constexpr int kOffMisc = kOffPairs + kPairBytes;
+constexpr int kOffRing = kLutBytes;
+constexpr int kOffRed = kOffRing + kRingBytes;
+constexpr int kOffMisc = kOffRed + kRedBytes;
 constexpr size_t kSmemBytes = kOffMisc + 64;
+
+// The dynamic shared memory of the decode kernels.  Hot-loop accesses index
+// this symbol directly with 32-bit offsets, so they compile to shared loads
+// with register + immediate addressing.
+extern __shared__ __align__(16) unsigned char g_dsmem[];
 
 struct SmemPtrs {
   unsigned char* lut;
-  float* act;
+  unsigned char* ring;
   float* red;
-  int* count;
-  int* pairs;
   int* misc;
 };
 
 __device__ __forceinline__ SmemPtrs carve(unsigned char* base) {
   SmemPtrs s;
   s.lut = base;
-  s.act = reinterpret_cast<float*>(base + kOffAct);
+  s.ring = base + kOffRing;
   s.red = reinterpret_cast<float*>(base + kOffRed);
-  s.count = reinterpret_cast<int*>(base + kOffCount);
-  s.pairs = reinterpret_cast<int*>(base + kOffPairs);
   s.misc = reinterpret_cast<int*>(base + kOffMisc);
   return s;
 }
 
-struct Route {
-  int e;    // routed expert of this CTA's slot, -1 if the slot is empty
-  int off;  // number of pairs routed to lower expert ids
-  int ne;   // number of pairs routed to e
+// Workspace of one decode call.
+struct DecodeWs {
+  float* x32;      // [T][H]   hidden states widened to fp32
+  float* h;        // [P][I]   SiLU(g) * u, by grouped pair position
+  float* y;        // [P][H]   expert output, by pair id
+  int* offsets;    // [E+1]    expert e owns grouped positions offsets[e] .. offsets[e+1]
+  int* perm;       // [P]      grouped position -> pair id
+  int* routed_gu;  // [E]      routed experts, gate_up bitwidth descending
+  int* routed_dn;  // [E]      routed experts, down bitwidth descending
+  int* ctl;        // [0] routed expert count, [1] gate_up tile counter, [2] down tile counter
+  int* arrive;     // [H/32]   per 64-row range: down tiles finished
 };
 
-// Whole-CTA: count pairs per expert, pick the slot-th routed expert (ascending
-// id), list its pairs ascending into s.pairs.
-__device__ Route route_slot(const LayerArgs& a, int slot, const SmemPtrs& s, bool report) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_pairs = a.T * a.k;
-  for (int e = tid; e < a.E; e += kThreads) s.count[e] = 0;
-  __syncthreads();
-  for (int p = tid; p < n_pairs; p += kThreads) {
-    const int e = a.topk_ids[p];
-    if (e >= 0 && e < a.E) {
-      atomicAdd(&s.count[e], 1);
-    } else if (report) {
-      latch_status(a.status, PW_ERR_BAD_EXPERT_ID);
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int routed = 0;
-    for (int base = 0; base < a.E; base += 32) {
-      const int e = base + lane;
-      routed += __popc(__ballot_sync(kFull, e < a.E && s.count[e] > 0));
-    }
-    if (lane == 0) s.misc[3] = routed;
-    int seen = 0, off = 0, found = -1;
-    for (int base = 0; base < a.E && found < 0; base += 32) {
-      const int e = base + lane;
-      const int c = (e < a.E) ? s.count[e] : 0;
-      const unsigned mask = __ballot_sync(kFull, c > 0);
-      const int n = __popc(mask);
-      int part;
-      if (slot < seen + n) {
-        const int want = slot - seen;
-        const bool mine = (c > 0) && (__popc(mask & ((1u << lane) - 1u)) == want);
-        const int src = __ffs(__ballot_sync(kFull, mine)) - 1;
-        found = base + src;
-        part = (lane < src) ? c : 0;
-      } else {
-        part = c;
-        seen += n;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
-      off += part;
-    }
-    if (lane == 0) {
-      s.misc[0] = found;
-      s.misc[1] = off;
-      s.misc[2] = (found >= 0) ? s.count[found] : 0;
-    }
-    if (found >= 0) {
-      int run = 0;
-      for (int c0 = 0; c0 < n_pairs; c0 += 32) {
-        const int p = c0 + lane;
-        const bool hit = (p < n_pairs) && (a.topk_ids[p] == found);
-        const unsigned m = __ballot_sync(kFull, hit);
-        if (hit) s.pairs[run + __popc(m & ((1u << lane) - 1u))] = p;
-        run += __popc(m);
-      }
-    }
-  }
-  __syncthreads();
-  Route r;
-  r.e = s.misc[0];
-  r.off = s.misc[1];
-  r.ne = s.misc[2];
-  return r;
+// Rows streamed by one pass: lane L of row slot g owns row
+// seg[g][L >> 4] + (L & 15), i.e. each slot is two 16-row segments.
+template <int R>
+struct PassRows {
+  int seg[R][2];
+};
+
+// One expert's share of a call.
+struct ExpertWork {
+  int e;    // expert id
+  int off;  // first grouped pair position of e
+  int ne;   // pairs routed to e
+};
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// LUT rows of the tile into the lane-private layout: row slot g, lane L,
-// entry v -> byte v*256 + g*128 + L*4, as fp32.  Each thread moves 8 fp16
-// entries (16 bytes); the stores of a warp hit 32 different banks.
-template <int Q, int R>
-__device__ __forceinline__ void load_luts(const uint16_t* lut, const int (&row0)[R],
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <int R>
+__device__ __forceinline__ int seg_base(const PassRows<R>& pr, int g, int seg) {
+  const int a = seg ? pr.seg[0][1] : pr.seg[0][0];
+  if (R == 1) return a;
+  const int b = seg ? pr.seg[R - 1][1] : pr.seg[R - 1][0];
+  return g ? b : a;
+}
+
+template <int NT>
+__device__ __forceinline__ const float* pick(const float* const (&xs)[NT], int tk) {
+  const float* p = xs[0];
+#pragma unroll
+  for (int i = 1; i < NT; ++i)
+    if (tk == i) p = xs[i];
+  return p;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// LUT rows of one pass into shared memory as fp32 (layouts above).  Each
+// thread moves 8 fp16 entries (16 bytes); a warp's stores hit 32 banks.
+template <int Q, int R, bool COMPACT>
+__device__ __forceinline__ void load_luts(const uint16_t* lut, const PassRows<R>& pr,
                                           const SmemPtrs& s) {
   constexpr int kEnt = 1 << Q;
   constexpr int kVecPerRow = kEnt / 8;
@@ -166,12 +173,16 @@ __device__ __forceinline__ void load_luts(const uint16_t* lut, const int (&row0)
   for (int g = 0; g < R; ++g) {
     for (int i = threadIdx.x; i < 32 * kVecPerRow; i += kThreads) {
       const int L = i & 31, vec = i >> 5;
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-          lut + static_cast<long long>(row0[g] + L) * kEnt + vec * 8));
+      const int row = seg_base<R>(pr, g, L >> 4) + (L & 15);
+      const uint4 raw =
+          __ldg(reinterpret_cast<const uint4*>(lut + static_cast<long long>(row) * kEnt + vec * 8));
       const __half* h = reinterpret_cast<const __half*>(&raw);
-      unsigned char* dst = s.lut + (vec * 8) * 256 + g * 128 + L * 4;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) *reinterpret_cast<float*>(dst + j * 256) = __half2float(h[j]);
+      for (int j = 0; j < 8; ++j) {
+        const int v = vec * 8 + j;
+        const int off = COMPACT ? v * 128 + L * 4 : v * 256 + g * 128 + L * 4;
+        *reinterpret_cast<float*>(g_dsmem + off) = __half2float(h[j]);
+      }
     }
   }
 }
@@ -188,15 +199,34 @@ __device__ __forceinline__ void byte_transpose4(uint32_t a0, uint32_t a1, uint32
   out[3] = __byte_perm(t1, t3, 0x7632);
 }
 
+// Multipliers for the bit transpose, passed as kernel parameters so that
+// the compiler keeps them as integer multiplies: x >> s == umulhi(x, 2^(32-s))
+// and x << s == x * 2^s, which run on the multiply-add pipe and leave the
+// logic pipe to the XOR / AND / byte-permute work.
+struct BitConsts {
+  uint32_t hi7, mul7;     // 2^25, 2^7 + 1
+  uint32_t hi14, mul14;   // 2^18, 2^14 + 1
+  uint32_t hi4, mul4;     // 2^28, 2^4
+};
+
 // Transpose of the 8x8 bit matrix held in (lo, hi): byte r = matrix row r,
-// bit c = column c  ->  byte c = column c, bit r = row r.  Three delta swaps.
-__device__ __forceinline__ void bit_transpose8(uint32_t& lo, uint32_t& hi) {
-  uint32_t t;
-  t = (lo ^ (lo >> 7)) & 0x00AA00AAu; lo ^= t ^ (t << 7);
-  t = (hi ^ (hi >> 7)) & 0x00AA00AAu; hi ^= t ^ (t << 7);
-  t = (lo ^ (lo >> 14)) & 0x0000CCCCu; lo ^= t ^ (t << 14);
-  t = (hi ^ (hi >> 14)) & 0x0000CCCCu; hi ^= t ^ (t << 14);
-  t = (lo ^ (hi << 4)) & 0xF0F0F0F0u; lo ^= t; hi ^= t >> 4;
+// bit c = column c  ->  byte c = column c, bit r = row r.  Two delta-swap
+// stages inside each half and one nibble exchange between the halves.  In a
+// delta swap the swapped bits t and t << s never overlap, so
+// x ^ t ^ (t << s) is x ^ (t * (2^s + 1)).
+__device__ __forceinline__ void delta_swap(uint32_t& x, uint32_t hi_mul, uint32_t mul, uint32_t m) {
+  const uint32_t t = (x ^ __umulhi(x, hi_mul)) & m;
+  x ^= t * mul;
+}
+
+__device__ __forceinline__ void bit_transpose8(uint32_t& lo, uint32_t& hi, const BitConsts& bc) {
+  delta_swap(lo, bc.hi7, bc.mul7, 0x00AA00AAu);
+  delta_swap(hi, bc.hi7, bc.mul7, 0x00AA00AAu);
+  delta_swap(lo, bc.hi14, bc.mul14, 0x0000CCCCu);
+  delta_swap(hi, bc.hi14, bc.mul14, 0x0000CCCCu);
+  const uint32_t l = lo;
+  lo = (lo & 0x0F0F0F0Fu) | ((hi * bc.mul4) & 0xF0F0F0F0u);
+  hi = (hi & 0xF0F0F0F0u) | (__umulhi(l, bc.hi4) & 0x0F0F0F0Fu);
 }
 
 // Q plane words of one row (P[0] = most significant plane) covering 32
@@ -204,7 +234,8 @@ __device__ __forceinline__ void bit_transpose8(uint32_t& lo, uint32_t& hi) {
 // is the index of column 4m + j.  Plane p feeds bit (Q-1-p) of the index;
 // for Q <= 4 half of the matrix is zero and the compiler folds it away.
 template <int Q>
-__device__ __forceinline__ void planes_to_index_bytes(const uint32_t (&P)[Q], uint32_t (&ib)[8]) {
+__device__ __forceinline__ void planes_to_index_bytes(const uint32_t (&P)[Q], uint32_t (&ib)[8],
+                                                      const BitConsts& bc) {
   uint32_t r[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) r[i] = (i < Q) ? P[Q - 1 - i] : 0u;
@@ -214,81 +245,138 @@ __device__ __forceinline__ void planes_to_index_bytes(const uint32_t (&P)[Q], ui
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
     uint32_t lo = A[b], hi = B[b];
-    bit_transpose8(lo, hi);
+    bit_transpose8(lo, hi, bc);
     ib[2 * b] = lo;
     ib[2 * b + 1] = hi;
   }
 }
 
-__device__ __forceinline__ float lane4(const float4& v, int j) {
-  return (j == 0) ? v.x : (j == 1) ? v.y : (j == 2) ? v.z : v.w;
+// The copies one lane issues for every word column: chunk c (16 bytes) of
+// a stage is plane p = (c/8)/R, row slot g = (c/8)%R, 16-row segment
+// (c/4)%2 and quarter c%4; it lands at stage byte c*16.  Its source is
+// planes + src_off + kw*N; the word offsets are fixed for a pass, so they are
+// computed once.  Activation chunk lane (< NT*8): token lane/8, 8 floats.
+template <int Q, int R, int NT>
+struct CopyPlan {
+  static constexpr int kChunks = (Q * R * 8 + 31) / 32;
+  uint32_t src_off[kChunks];
+  const float* x_src;   // token row + part offset (column 0)
+  uint32_t x_bytes;     // 16, or 0 to zero-fill an absent token
+};
+
+template <int Q, int R, int NT>
+__device__ __forceinline__ CopyPlan<Q, R, NT> make_copy_plan(long long plane_stride,
+                                                             const PassRows<R>& pr,
+                                                             const float* const (&xs)[NT],
+                                                             int nt, int lane) {
+  CopyPlan<Q, R, NT> cp;
+#pragma unroll
+  for (int i = 0; i < CopyPlan<Q, R, NT>::kChunks; ++i) {
+    const int c = i * 32 + lane;
+    const int pg = c >> 3, seg = (c >> 2) & 1, part = c & 3;
+    const int p = pg / R, g = pg % R;
+    cp.src_off[i] = (c < Q * R * 8)
+                        ? static_cast<uint32_t>(p * plane_stride + seg_base<R>(pr, g, seg) + part * 4)
+                        : 0u;
+  }
+  const int tk = lane >> 3, part = lane & 7;
+  const bool live = lane < NT * 8 && tk < nt;
+  cp.x_src = (live ? pick<NT>(xs, tk) : xs[0]) + part * 4;
+  cp.x_bytes = live ? 16u : 0u;
+  return cp;
 }
 
-// Partial dot products of this lane's R rows over the warp's words
-// [kw_lo, kw_hi), for NT tokens whose activations `load_chunk` stages per
-// kCW-word chunk.  Plane words are loaded one word column ahead.
-template <int Q, int R, int NT, class Loader>
-__device__ __forceinline__ void rows_dot(const uint32_t* planes, long long plane_stride, int N,
-                                         const int (&row)[R], int kw_lo, int kw_hi,
-                                         const SmemPtrs& s, const Loader& load_chunk,
-                                         float (&acc)[R][NT]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float* act = s.act + warp * (kTG * kCC);
+// Start the asynchronous copies of word column kw of every streamed row and
+// of the matching 32 activations of each token into one ring stage.
+template <int Q, int R, int NT>
+__device__ __forceinline__ void issue_column(uint32_t stage, const uint32_t* planes, long long N,
+                                             const CopyPlan<Q, R, NT>& cp, int kw, int lane) {
+  const uint32_t col = static_cast<uint32_t>(kw * N);
+#pragma unroll
+  for (int i = 0; i < CopyPlan<Q, R, NT>::kChunks; ++i) {
+    const int c = i * 32 + lane;
+    if (c < Q * R * 8) cp_async16(stage + c * 16, planes + (cp.src_off[i] + col), 16);
+  }
+  if (lane < NT * 8)
+    cp_async16(stage + kStagePlaneBytes + lane * 16, cp.x_src + (cp.x_bytes ? kw * 32 : 0),
+               cp.x_bytes);
+}
+
+// One word column from a ring stage: rebuild the 32 indices of each row,
+// look them up, and accumulate against NT tokens (packed fp32 pairs).
+template <int Q, int R, int NT, bool COMPACT>
+__device__ __forceinline__ void compute_column(uint32_t stage, int lane, const BitConsts& bc,
+                                               float2 (&acc)[R][NT]) {
+  uint32_t cur[R][Q];
+#pragma unroll
+  for (int p = 0; p < Q; ++p)
+#pragma unroll
+    for (int g = 0; g < R; ++g)
+      cur[g][p] = *reinterpret_cast<const uint32_t*>(g_dsmem + stage + (p * R + g) * 128 + lane * 4);
+  uint32_t ib[R][8];
+#pragma unroll
+  for (int g = 0; g < R; ++g) planes_to_index_bytes<Q>(cur[g], ib[g], bc);
+  const float* xa = reinterpret_cast<const float*>(g_dsmem + stage + kStagePlaneBytes);
   uint32_t lb[R];
 #pragma unroll
-  for (int g = 0; g < R; ++g) lb[g] = (static_cast<uint32_t>(g) << 7) | (lane << 2);
-#pragma unroll
   for (int g = 0; g < R; ++g)
+    lb[g] = COMPACT ? (static_cast<uint32_t>(lane) << 3)
+                    : ((static_cast<uint32_t>(g) << 7) | (static_cast<uint32_t>(lane) << 2));
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[g][t] = 0.f;
-  if (kw_lo >= kw_hi) return;
-  uint32_t nxt[R][Q];
+  for (int m = 0; m < 8; ++m) {
+    float4 xv[NT];
 #pragma unroll
-  for (int g = 0; g < R; ++g)
+    for (int tk = 0; tk < NT; ++tk) xv[tk] = *reinterpret_cast<const float4*>(xa + tk * 32 + 4 * m);
 #pragma unroll
-    for (int p = 0; p < Q; ++p)
-      nxt[g][p] = __ldg(planes + p * plane_stride + static_cast<long long>(kw_lo) * N + row[g]);
-  for (int kw0 = kw_lo; kw0 < kw_hi; kw0 += kCW) {
-    const int nw = min(kCW, kw_hi - kw0);
-    __syncwarp();
-    load_chunk(act, kw0 * 32, nw * 32);
-    __syncwarp();
-    for (int ww = 0; ww < nw; ++ww) {
-      uint32_t cur[R][Q];
+    for (int g = 0; g < R; ++g) {
+      float w[4];
 #pragma unroll
-      for (int g = 0; g < R; ++g)
-#pragma unroll
-        for (int p = 0; p < Q; ++p) cur[g][p] = nxt[g][p];
-      const int kn = kw0 + ww + 1;
-      if (kn < kw_hi) {
-#pragma unroll
-        for (int g = 0; g < R; ++g)
-#pragma unroll
-          for (int p = 0; p < Q; ++p)
-            nxt[g][p] = __ldg(planes + p * plane_stride + static_cast<long long>(kn) * N + row[g]);
+      for (int j = 0; j < 4; ++j) {
+        uint32_t off = __byte_perm(ib[g][m], lb[g], 0x6504 | (j << 4));
+        if (COMPACT) off >>= 1;
+        w[j] = *reinterpret_cast<const float*>(g_dsmem + off);
       }
-      uint32_t ib[R][8];
 #pragma unroll
-      for (int g = 0; g < R; ++g) planes_to_index_bytes<Q>(cur[g], ib[g]);
-      const float* xa = act + ww * 32;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        float4 xv[NT];
-#pragma unroll
-        for (int tk = 0; tk < NT; ++tk)
-          xv[tk] = *reinterpret_cast<const float4*>(xa + tk * kCC + 4 * m);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-          for (int g = 0; g < R; ++g) {
-            const uint32_t off = __byte_perm(ib[g][m], lb[g], 0x6504 | (j << 4));
-            const float w = *reinterpret_cast<const float*>(s.lut + off);
-#pragma unroll
-            for (int tk = 0; tk < NT; ++tk) acc[g][tk] = fmaf(lane4(xv[tk], j), w, acc[g][tk]);
-          }
-        }
+      for (int tk = 0; tk < NT; ++tk) {
+        acc[g][tk] = __ffma2_rn(make_float2(w[0], w[1]), make_float2(xv[tk].x, xv[tk].y), acc[g][tk]);
+        acc[g][tk] = __ffma2_rn(make_float2(w[2], w[3]), make_float2(xv[tk].z, xv[tk].w), acc[g][tk]);
       }
     }
+  }
+}
+
+// Partial dot products of this lane's rows over the warp's word columns
+// [kw_lo, kw_hi), streamed through the warp's kStages-deep cp.async ring.
+template <int Q, int R, int NT, bool COMPACT>
+__device__ __forceinline__ void rows_dot(const uint32_t* planes, long long plane_stride, long long N,
+                                         const PassRows<R>& pr, int kw_lo, int kw_hi,
+                                         const float* const (&xs)[NT], int nt, const SmemPtrs& s,
+                                         const BitConsts& bc, float2 (&acc)[R][NT]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int g = 0; g < R; ++g)
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[g][t] = make_float2(0.f, 0.f);
+  const int n = kw_hi - kw_lo;
+  if (n <= 0) return;
+  const uint32_t ring = kOffRing + warp * (kStages * kStageBytes);   // offset in g_dsmem
+  const uint32_t ring_s = smem_u32(g_dsmem) + ring;
+  const CopyPlan<Q, R, NT> plan = make_copy_plan<Q, R, NT>(plane_stride, pr, xs, nt, lane);
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) {
+    if (i < n) issue_column<Q, R, NT>(ring_s + i * kStageBytes, planes, N, plan, kw_lo + i, lane);
+    cp_async_commit();
+  }
+  for (int i = 0; i < n; ++i) {
+    const int pf = i + kStages - 1;
+    if (pf < n)
+      issue_column<Q, R, NT>(ring_s + (pf % kStages) * kStageBytes, planes, N, plan, kw_lo + pf,
+                             lane);
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    compute_column<Q, R, NT, COMPACT>(ring + (i % kStages) * kStageBytes, lane, bc, acc);
+    __syncwarp();
   }
 }
 
@@ -298,228 +386,390 @@ __device__ __forceinline__ void warp_range(int KW, int& lo, int& hi) {
   hi = ((warp + 1) * KW) / kWarps;
 }
 
+
+// Broadcast the next tile id from a global counter to the whole CTA.
+__device__ __forceinline__ int next_tile(int* counter, int* slot) {
+  if (threadIdx.x == 0) *slot = atomicAdd(counter, 1);
+  __syncthreads();
+  const int t = *slot;
+  __syncthreads();
+  return t;
+}
+
 // ---------------------------------------------------------------- gate_up
 
-template <int Q, int NT>
-__device__ void gateup_group(const LayerArgs& a, const Route& r, const pw_block_entry& ent,
-                             int i0, int g0, int nt, const SmemPtrs& s, float* h_ws) {
+// One token group of one pass.  Paired passes (R = 2): slot 0 = gate rows
+// hcol0 + L, slot 1 = up rows I + hcol0 + L.  Compact passes (R = 1): lanes
+// 0-15 gate rows hcol0 + L, lanes 16-31 the matching up rows.
+template <int Q, int R, bool COMPACT, int NT>
+__device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
+                             const pw_block_entry& ent, const PassRows<R>& pr, int hcol0, int g0,
+                             int nt, const SmemPtrs& s, const BitConsts& bc) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int KW = a.H / 32;
-  const int N = 2 * a.I;
-  const long long plane_stride = static_cast<long long>(N) * KW;
-  const int row[2] = {i0 + lane, a.I + i0 + lane};
+  const long long N = 2LL * a.I;
   int lo, hi;
   warp_range(KW, lo, hi);
-  int tok[NT];
+  const float* xs[NT];
 #pragma unroll
-  for (int tk = 0; tk < NT; ++tk) tok[tk] = (tk < nt) ? s.pairs[g0 + tk] / a.k : -1;
-  auto loader = [&](float* act, int c0, int cols) {
-    const int c = lane * 4;
+  for (int tk = 0; tk < NT; ++tk)
+    xs[tk] = w.x32 + static_cast<long long>(w.perm[ex.off + g0 + min(tk, nt - 1)] / a.k) * a.H;
+  float2 acc[R][NT];
+  rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc);
 #pragma unroll
-    for (int tk = 0; tk < NT; ++tk) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (tok[tk] >= 0 && c < cols) {
-        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(
-            a.hidden + static_cast<long long>(tok[tk]) * a.H + c0 + c));
-        v = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
-                        __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
-      }
-      *reinterpret_cast<float4*>(act + tk * kCC + c) = v;
-    }
-  };
-  float acc[2][NT];
-  rows_dot<Q, 2, NT>(ent.planes, plane_stride, N, row, lo, hi, s, loader, acc);
+  for (int tk = 0; tk < NT; ++tk)
 #pragma unroll
-  for (int tk = 0; tk < NT; ++tk) {
-    s.red[((warp * kTG + tk) * 2 + 0) * 32 + lane] = acc[0][tk];
-    s.red[((warp * kTG + tk) * 2 + 1) * 32 + lane] = acc[1][tk];
-  }
+    for (int g = 0; g < R; ++g)
+      s.red[((warp * kTG + tk) * 2 + g) * 32 + lane] = acc[g][tk].x + acc[g][tk].y;
   __syncthreads();
   if (threadIdx.x < 32 * nt) {
     const int tk = threadIdx.x >> 5;
-    float g = 0.f, u = 0.f;
+    float v0 = 0.f, v1 = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      g += s.red[((w * kTG + tk) * 2 + 0) * 32 + lane];
-      u += s.red[((w * kTG + tk) * 2 + 1) * 32 + lane];
+    for (int ww = 0; ww < kWarps; ++ww) {
+      v0 += s.red[((ww * kTG + tk) * 2 + 0) * 32 + lane];
+      if (R == 2) v1 += s.red[((ww * kTG + tk) * 2 + 1) * 32 + lane];
     }
-    const float h = g / (1.f + expf(-g)) * u;
-    h_ws[static_cast<long long>(r.off + g0 + tk) * a.I + i0 + lane] = h;
+    if (R == 1) v1 = __shfl_xor_sync(kFull, v0, 16);
+    const int width = (R == 2) ? 32 : 16;
+    if (lane < width) {
+      const float h = v0 / (1.f + expf(-v0)) * v1;
+      w.h[static_cast<long long>(ex.off + g0 + tk) * a.I + hcol0 + lane] = h;
+    }
   }
   __syncthreads();
+}
+
+template <int Q, int R, bool COMPACT>
+__device__ void gateup_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
+                            const pw_block_entry& ent, const PassRows<R>& pr, int hcol0,
+                            const SmemPtrs& s, const BitConsts& bc) {
+  __syncthreads();  // the previous pass is done with the LUT region
+  load_luts<Q, R, COMPACT>(ent.lut, pr, s);
+  __syncthreads();
+  for (int g0 = 0; g0 < ex.ne; g0 += kTG) {
+    const int nt = min(kTG, ex.ne - g0);
+    if (nt == 1) gateup_group<Q, R, COMPACT, 1>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc);
+    else if (nt == 2) gateup_group<Q, R, COMPACT, 2>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc);
+    else gateup_group<Q, R, COMPACT, 4>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc);
+  }
 }
 
 template <int Q>
-__device__ void gateup_tile(const LayerArgs& a, const Route& r, const pw_block_entry& ent,
-                            int i0, const SmemPtrs& s, float* h_ws) {
-  const int row0[2] = {i0, a.I + i0};
-  load_luts<Q, 2>(ent.lut, row0, s);
-  __syncthreads();
-  for (int g0 = 0; g0 < r.ne; g0 += kTG) {
-    const int nt = min(kTG, r.ne - g0);
-    if (nt == 1) gateup_group<Q, 1>(a, r, ent, i0, g0, nt, s, h_ws);
-    else if (nt == 2) gateup_group<Q, 2>(a, r, ent, i0, g0, nt, s, h_ws);
-    else gateup_group<Q, 4>(a, r, ent, i0, g0, nt, s, h_ws);
+__device__ void gateup_tile(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
+                            const pw_block_entry& ent, int i0, const SmemPtrs& s,
+                            const BitConsts& bc) {
+  if (Q == 8) {
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      const int i = i0 + 16 * half;
+      PassRows<1> pr;
+      pr.seg[0][0] = i;
+      pr.seg[0][1] = a.I + i;
+      gateup_pass<8, 1, true>(a, w, ex, ent, pr, i, s, bc);
+    }
+  } else {
+    PassRows<2> pr;
+    pr.seg[0][0] = i0;
+    pr.seg[0][1] = i0 + 16;
+    pr.seg[1][0] = a.I + i0;
+    pr.seg[1][1] = a.I + i0 + 16;
+    gateup_pass<Q, 2, false>(a, w, ex, ent, pr, i0, s, bc);
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerArgs a, float* h_ws,
-                                                                    int* tile_count) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  const SmemPtrs s = carve(smem_raw);
-  // Zero the output (covers calls where no pair has a valid expert) and the
-  // down kernel's per-tile arrival counters; the down kernel runs after this
-  // grid has completed.
-  {
-    const long long total = static_cast<long long>(a.T) * a.H;
-    const long long cta = blockIdx.y * static_cast<long long>(gridDim.x) + blockIdx.x;
-    const long long stride = static_cast<long long>(gridDim.x) * gridDim.y * kThreads;
-    for (long long i = cta * kThreads + threadIdx.x; i < total; i += stride) a.out[i] = 0.f;
-    const int n_tiles = (a.H + kDownRows - 1) / kDownRows;
-    for (long long i = cta * kThreads + threadIdx.x; i < n_tiles; i += stride) tile_count[i] = 0;
-  }
-  const bool report = blockIdx.x == 0;
-  const Route r = route_slot(a, blockIdx.y, s, report);
-  if (r.e < 0) return;
-  const pw_block_entry ent = a.table[2 * r.e];
-  if (ent.state != PW_PAGE_GPU) {
-    if (report) latch_status(a.status, PW_ERR_PAGE_NOT_RESIDENT);
-    return;
-  }
-  const int i0 = blockIdx.x * kPairsPerTile;
-  switch (ent.q) {
-    case 3: gateup_tile<3>(a, r, ent, i0, s, h_ws); break;
-    case 4: gateup_tile<4>(a, r, ent, i0, s, h_ws); break;
-    case 5: gateup_tile<5>(a, r, ent, i0, s, h_ws); break;
-    case 6: gateup_tile<6>(a, r, ent, i0, s, h_ws); break;
-    case 8: gateup_tile<8>(a, r, ent, i0, s, h_ws); break;
-    default:
-      if (report) latch_status(a.status, PW_ERR_UNSUPPORTED_Q);
+__global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerArgs a,
+                                                                    const DecodeWs w,
+                                                                    const BitConsts bc) {
+  const SmemPtrs s = carve(g_dsmem);
+  grid_dependency_wait();      // routing and fp32 hidden states are ready
+  allow_dependent_launch();    // the down kernel may start loading as CTAs retire
+  const int tpe = a.I / kPairsPerTile;
+  const int total = w.ctl[0] * tpe;
+  for (;;) {
+    const int t = next_tile(&w.ctl[1], &s.misc[0]);
+    if (t >= total) break;
+    const int slot = t / tpe, x = t - slot * tpe;
+    ExpertWork ex;
+    ex.e = w.routed_gu[slot];
+    ex.off = w.offsets[ex.e];
+    ex.ne = w.offsets[ex.e + 1] - ex.off;
+    const pw_block_entry ent = a.table[2 * ex.e];
+    if (ent.state != PW_PAGE_GPU) {
+      if (x == 0 && threadIdx.x == 0) latch_status(a.status, PW_ERR_PAGE_NOT_RESIDENT);
+      continue;
+    }
+    switch (ent.q) {
+      case 3: gateup_tile<3>(a, w, ex, ent, x * kPairsPerTile, s, bc); break;
+      case 4: gateup_tile<4>(a, w, ex, ent, x * kPairsPerTile, s, bc); break;
+      case 5: gateup_tile<5>(a, w, ex, ent, x * kPairsPerTile, s, bc); break;
+      case 6: gateup_tile<6>(a, w, ex, ent, x * kPairsPerTile, s, bc); break;
+      case 8: gateup_tile<8>(a, w, ex, ent, x * kPairsPerTile, s, bc); break;
+      default:
+        if (x == 0 && threadIdx.x == 0) latch_status(a.status, PW_ERR_UNSUPPORTED_Q);
+    }
   }
 }
 
 // ---------------------------------------------------------------- down
 
-template <int Q, int R, int NT>
-__device__ void down_group(const LayerArgs& a, const Route& r, const pw_block_entry& ent,
-                           int n0, int g0, int nt, const SmemPtrs& s, const float* h_ws,
-                           float* y_ws) {
+template <int Q, int R, bool COMPACT, int NT>
+__device__ void down_group(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
+                           const pw_block_entry& ent, const PassRows<R>& pr, int g0, int nt,
+                           const SmemPtrs& s, const BitConsts& bc) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int KW = a.I / 32;
-  const int N = a.H;
-  const long long plane_stride = static_cast<long long>(N) * KW;
-  int row[R];
-#pragma unroll
-  for (int g = 0; g < R; ++g) row[g] = n0 + 32 * g + lane;
+  const long long N = a.H;
   int lo, hi;
   warp_range(KW, lo, hi);
-  auto loader = [&](float* act, int c0, int cols) {
-    const int c = lane * 4;
+  const float* xs[NT];
 #pragma unroll
-    for (int tk = 0; tk < NT; ++tk) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (tk < nt && c < cols)
-        v = *reinterpret_cast<const float4*>(h_ws + static_cast<long long>(r.off + g0 + tk) * a.I +
-                                             c0 + c);
-      *reinterpret_cast<float4*>(act + tk * kCC + c) = v;
-    }
-  };
-  float acc[R][NT];
-  rows_dot<Q, R, NT>(ent.planes, plane_stride, N, row, lo, hi, s, loader, acc);
+  for (int tk = 0; tk < NT; ++tk)
+    xs[tk] = w.h + static_cast<long long>(ex.off + g0 + min(tk, nt - 1)) * a.I;
+  float2 acc[R][NT];
+  rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc);
 #pragma unroll
   for (int tk = 0; tk < NT; ++tk)
 #pragma unroll
-    for (int g = 0; g < R; ++g) s.red[((warp * kTG + tk) * 2 + g) * 32 + lane] = acc[g][tk];
+    for (int g = 0; g < R; ++g)
+      s.red[((warp * kTG + tk) * 2 + g) * 32 + lane] = acc[g][tk].x + acc[g][tk].y;
   __syncthreads();
   for (int i = threadIdx.x; i < 32 * R * nt; i += kThreads) {
     const int L = i & 31, g = (i >> 5) % R, tk = (i >> 5) / R;
     float y = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) y += s.red[((w * kTG + tk) * 2 + g) * 32 + L];
-    y_ws[static_cast<long long>(s.pairs[g0 + tk]) * a.H + n0 + 32 * g + L] = y;
+    for (int ww = 0; ww < kWarps; ++ww) y += s.red[((ww * kTG + tk) * 2 + g) * 32 + L];
+    const int row = seg_base<R>(pr, g, L >> 4) + (L & 15);
+    w.y[static_cast<long long>(w.perm[ex.off + g0 + tk]) * a.H + row] = y;
   }
   __syncthreads();
 }
 
-template <int Q, int R>
-__device__ void down_tile(const LayerArgs& a, const Route& r, const pw_block_entry& ent, int n0,
-                          const SmemPtrs& s, const float* h_ws, float* y_ws) {
-  int row0[R];
-#pragma unroll
-  for (int g = 0; g < R; ++g) row0[g] = n0 + 32 * g;
-  load_luts<Q, R>(ent.lut, row0, s);
+template <int Q, int R, bool COMPACT>
+__device__ void down_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
+                          const pw_block_entry& ent, const PassRows<R>& pr, const SmemPtrs& s,
+                          const BitConsts& bc) {
   __syncthreads();
-  for (int g0 = 0; g0 < r.ne; g0 += kTG) {
-    const int nt = min(kTG, r.ne - g0);
-    if (nt == 1) down_group<Q, R, 1>(a, r, ent, n0, g0, nt, s, h_ws, y_ws);
-    else if (nt == 2) down_group<Q, R, 2>(a, r, ent, n0, g0, nt, s, h_ws, y_ws);
-    else down_group<Q, R, 4>(a, r, ent, n0, g0, nt, s, h_ws, y_ws);
+  load_luts<Q, R, COMPACT>(ent.lut, pr, s);
+  grid_dependency_wait();   // h is complete from here on
+  __syncthreads();
+  for (int g0 = 0; g0 < ex.ne; g0 += kTG) {
+    const int nt = min(kTG, ex.ne - g0);
+    if (nt == 1) down_group<Q, R, COMPACT, 1>(a, w, ex, ent, pr, g0, nt, s, bc);
+    else if (nt == 2) down_group<Q, R, COMPACT, 2>(a, w, ex, ent, pr, g0, nt, s, bc);
+    else down_group<Q, R, COMPACT, 4>(a, w, ex, ent, pr, g0, nt, s, bc);
   }
 }
 
-template <int R>
-__device__ void down_dispatch(const LayerArgs& a, const Route& r, const pw_block_entry& ent,
-                              int n0, const SmemPtrs& s, const float* h_ws, float* y_ws) {
-  switch (ent.q) {
-    case 3: down_tile<3, R>(a, r, ent, n0, s, h_ws, y_ws); break;
-    case 4: down_tile<4, R>(a, r, ent, n0, s, h_ws, y_ws); break;
-    case 5: down_tile<5, R>(a, r, ent, n0, s, h_ws, y_ws); break;
-    case 6: down_tile<6, R>(a, r, ent, n0, s, h_ws, y_ws); break;
-    default: down_tile<8, R>(a, r, ent, n0, s, h_ws, y_ws); break;
-  }
-}
-
-// Pairs of an expert that cannot be computed contribute zero.
-__device__ void zero_pairs(const LayerArgs& a, const Route& r, int n0, int rows,
-                           const SmemPtrs& s, float* y_ws) {
-  for (int i = threadIdx.x; i < r.ne * rows; i += kThreads)
-    y_ws[static_cast<long long>(s.pairs[i / rows]) * a.H + n0 + (i % rows)] = 0.f;
-}
-
-__global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArgs a, const float* h_ws,
-                                                                  float* y_ws, int* tile_count) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  const SmemPtrs s = carve(smem_raw);
-  const Route r = route_slot(a, blockIdx.y, s, false);
-  if (r.e < 0) return;
-  const pw_block_entry gu = a.table[2 * r.e];
-  const pw_block_entry ent = a.table[2 * r.e + 1];
-  const bool report = blockIdx.x == 0;
-  const int n0 = blockIdx.x * kDownRows;
-  const int rows = min(kDownRows, a.H - n0);   // 64, or 32 on a ragged last tile
-  if (gu.state != PW_PAGE_GPU || ent.state != PW_PAGE_GPU) {
-    if (report) latch_status(a.status, PW_ERR_PAGE_NOT_RESIDENT);
-    zero_pairs(a, r, n0, rows, s, y_ws);
-  } else if (!supported_q(gu.q) || !supported_q(ent.q)) {
-    if (report && !supported_q(ent.q)) latch_status(a.status, PW_ERR_UNSUPPORTED_Q);
-    zero_pairs(a, r, n0, rows, s, y_ws);  // an unusable block: this expert contributes 0
-  } else if (rows == kDownRows) {
-    down_dispatch<2>(a, r, ent, n0, s, h_ws, y_ws);
-  } else {
-    down_dispatch<1>(a, r, ent, n0, s, h_ws, y_ws);
-  }
-  // Arrival: the last of the routed experts' CTAs on this row tile combines.
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int n_routed = s.misc[3];
-    const int old = atomicAdd(&tile_count[blockIdx.x], 1);
-    s.misc[4] = (old == n_routed - 1);
-    if (old == n_routed - 1) tile_count[blockIdx.x] = 0;  // ready for the next call
-  }
-  __syncthreads();
-  if (!s.misc[4]) return;
-  __threadfence();
-  for (int i = threadIdx.x; i < a.T * rows; i += kThreads) {
-    const int t = i / rows, n = n0 + i % rows;
-    float acc = 0.f;
-    for (int j = 0; j < a.k; ++j) {
-      const int p = t * a.k + j;
-      const int e = a.topk_ids[p];
-      if (e < 0 || e >= a.E) continue;
-      acc = fmaf(a.topk_weights[p], __ldcg(y_ws + static_cast<long long>(p) * a.H + n), acc);
+// A down tile of `rows` (64, or 32 on a ragged last tile) rows from n0.
+template <int Q>
+__device__ void down_tile(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
+                          const pw_block_entry& ent, int n0, int rows, const SmemPtrs& s,
+                          const BitConsts& bc) {
+  if (Q == 8 || rows == 32) {
+#pragma unroll 1
+    for (int grp = 0; grp < rows / 32; ++grp) {
+      PassRows<1> pr;
+      pr.seg[0][0] = n0 + 32 * grp;
+      pr.seg[0][1] = n0 + 32 * grp + 16;
+      if (Q == 8) down_pass<8, 1, true>(a, w, ex, ent, pr, s, bc);
+      else down_pass<Q, 1, false>(a, w, ex, ent, pr, s, bc);
     }
-    a.out[static_cast<long long>(t) * a.H + n] = acc;
+  } else {
+    PassRows<2> pr;
+    pr.seg[0][0] = n0;
+    pr.seg[0][1] = n0 + 16;
+    pr.seg[1][0] = n0 + 32;
+    pr.seg[1][1] = n0 + 48;
+    down_pass<Q, 2, false>(a, w, ex, ent, pr, s, bc);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArgs a,
+                                                                  const DecodeWs w,
+                                                                  const BitConsts bc) {
+  const SmemPtrs s = carve(g_dsmem);
+  // Routing (from the prep launch, which finished before the gate_up
+  // kernel allowed this launch) is readable now; h only after the wait.
+  const int n_routed = w.ctl[0];
+  const int tpe = (a.H + kDownRows - 1) / kDownRows;
+  const int total = n_routed * tpe;
+  for (;;) {
+    const int t = next_tile(&w.ctl[2], &s.misc[0]);
+    if (t >= total) break;
+    const int slot = t / tpe, x = t - slot * tpe;
+    ExpertWork ex;
+    ex.e = w.routed_dn[slot];
+    ex.off = w.offsets[ex.e];
+    ex.ne = w.offsets[ex.e + 1] - ex.off;
+    const pw_block_entry gu = a.table[2 * ex.e];
+    const pw_block_entry ent = a.table[2 * ex.e + 1];
+    const int n0 = x * kDownRows;
+    const int rows = min(kDownRows, a.H - n0);   // 64, or 32 on a ragged last range
+    if (gu.state != PW_PAGE_GPU || ent.state != PW_PAGE_GPU || !supported_q(gu.q) ||
+        !supported_q(ent.q)) {
+      // this expert contributes zero; gate_up skipped it (h is not valid)
+      if (x == 0 && threadIdx.x == 0) {
+        if (gu.state != PW_PAGE_GPU || ent.state != PW_PAGE_GPU)
+          latch_status(a.status, PW_ERR_PAGE_NOT_RESIDENT);
+        else if (!supported_q(ent.q))
+          latch_status(a.status, PW_ERR_UNSUPPORTED_Q);
+      }
+      for (int i = threadIdx.x; i < ex.ne * rows; i += kThreads)
+        w.y[static_cast<long long>(w.perm[ex.off + i / rows]) * a.H + n0 + (i % rows)] = 0.f;
+    } else {
+      switch (ent.q) {
+        case 3: down_tile<3>(a, w, ex, ent, n0, rows, s, bc); break;
+        case 4: down_tile<4>(a, w, ex, ent, n0, rows, s, bc); break;
+        case 5: down_tile<5>(a, w, ex, ent, n0, rows, s, bc); break;
+        case 6: down_tile<6>(a, w, ex, ent, n0, rows, s, bc); break;
+        default: down_tile<8>(a, w, ex, ent, n0, rows, s, bc); break;
+      }
+    }
+    // Arrival: the last routed expert to finish this row range combines it.
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s.misc[1] = (atomicAdd(&w.arrive[x], 1) == n_routed - 1);
+    __syncthreads();
+    if (s.misc[1]) {
+      __threadfence();
+      for (int i = threadIdx.x; i < a.T * rows; i += kThreads) {
+        const int tt = i / rows, n = n0 + i % rows;
+        float acc = 0.f;
+        for (int j = 0; j < a.k; ++j) {
+          const int p = tt * a.k + j;
+          const int e = a.topk_ids[p];
+          if (e < 0 || e >= a.E) continue;
+          acc = fmaf(a.topk_weights[p], __ldcg(w.y + static_cast<long long>(p) * a.H + n), acc);
+        }
+        a.out[static_cast<long long>(tt) * a.H + n] = acc;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- prep
+
+__device__ __forceinline__ int q_class(int q) {
+  return q == 8 ? 0 : q == 6 ? 1 : q == 5 ? 2 : q == 4 ? 3 : q == 3 ? 4 : 5;
+}
+
+// CTA 0: stable grouping of pairs by expert (offsets, perm), routed-expert
+// lists ordered by bitwidth class (largest first; order inside a class does
+// not matter), counters reset.  Other CTAs: hidden -> fp32 and out = 0.
+__global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerArgs a,
+                                                                   const DecodeWs w) {
+  allow_dependent_launch();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (blockIdx.x != 0) {
+    const long long n4 = static_cast<long long>(a.T) * a.H / 4;
+    const long long stride = static_cast<long long>(gridDim.x - 1) * kPrepThreads;
+    for (long long i = static_cast<long long>(blockIdx.x - 1) * kPrepThreads + tid; i < n4;
+         i += stride) {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.hidden) + i);
+      reinterpret_cast<float4*>(w.x32)[i] =
+          make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+      reinterpret_cast<float4*>(a.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+  extern __shared__ int psm[];
+  const int E = a.E, P = a.T * a.k;
+  int* count = psm;                 // [E]
+  int* base = count + E;            // [E]
+  int* wcnt = base + E;             // [kPrepWarps][E]
+  __shared__ int s_warp_sum[kPrepWarps];
+  __shared__ int s_bucket[2][8];
+  for (int e = tid; e < E; e += kPrepThreads) count[e] = 0;
+  for (int i = tid; i < kPrepWarps * E; i += kPrepThreads) wcnt[i] = 0;
+  if (tid < 16) (&s_bucket[0][0])[tid] = 0;
+  for (int i = tid; i < (a.H + 31) / 32; i += kPrepThreads) w.arrive[i] = 0;
+  __syncthreads();
+  for (int p = tid; p < P; p += kPrepThreads) {
+    const int e = a.topk_ids[p];
+    if (e >= 0 && e < E) atomicAdd(&count[e], 1);
+    else latch_status(a.status, PW_ERR_BAD_EXPERT_ID);
+  }
+  __syncthreads();
+  // exclusive scan of count -> base / offsets
+  const int per = (E + kPrepThreads - 1) / kPrepThreads;
+  const int lo = min(E, tid * per), hi = min(E, lo + per);
+  int run = 0;
+  for (int e = lo; e < hi; ++e) run += count[e];
+  int incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_warp_sum[warp] = incl;
+  __syncthreads();
+  int before = incl - run;
+  for (int ww = 0; ww < warp; ++ww) before += s_warp_sum[ww];
+  for (int e = lo; e < hi; ++e) {
+    base[e] = before;
+    w.offsets[e] = before;
+    before += count[e];
+  }
+  if (tid == kPrepThreads - 1) {
+    int total = 0;
+    for (int ww = 0; ww < kPrepWarps; ++ww) total += s_warp_sum[ww];
+    w.offsets[E] = total;
+  }
+  // routed experts by bitwidth class
+  for (int e = tid; e < E; e += kPrepThreads) {
+    if (count[e] > 0) {
+      atomicAdd(&s_bucket[0][q_class(a.table[2 * e].q)], 1);
+      atomicAdd(&s_bucket[1][q_class(a.table[2 * e + 1].q)], 1);
+    }
+  }
+  __syncthreads();
+  if (tid < 2) {
+    int acc = 0;
+    for (int c = 0; c < 6; ++c) {
+      const int n = s_bucket[tid][c];
+      s_bucket[tid][c] = acc;
+      acc += n;
+    }
+    if (tid == 0) {
+      w.ctl[0] = acc;
+      w.ctl[1] = 0;
+      w.ctl[2] = 0;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kPrepThreads) {
+    if (count[e] > 0) {
+      w.routed_gu[atomicAdd(&s_bucket[0][q_class(a.table[2 * e].q)], 1)] = e;
+      w.routed_dn[atomicAdd(&s_bucket[1][q_class(a.table[2 * e + 1].q)], 1)] = e;
+    }
+  }
+  // stable placement: rank among same-expert lanes (match), earlier warps of
+  // the chunk (per-warp counts) and earlier chunks (running base)
+  for (int c0 = 0; c0 < P; c0 += kPrepThreads) {
+    const int p = c0 + tid;
+    const int e = (p < P) ? a.topk_ids[p] : -1;
+    const bool valid = (e >= 0 && e < E);
+    const unsigned peers = __match_any_sync(kFull, valid ? e : -1);
+    const unsigned lower = peers & ((1u << lane) - 1u);
+    if (valid && lower == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int pos = base[e] + __popc(lower);
+      for (int ww = 0; ww < warp; ++ww) pos += wcnt[ww * E + e];
+      w.perm[pos] = p;
+    }
+    __syncthreads();
+    for (int x = tid; x < E; x += kPrepThreads) {
+      int add = 0;
+      for (int ww = 0; ww < kPrepWarps; ++ww) {
+        add += wcnt[ww * E + x];
+        wcnt[ww * E + x] = 0;
+      }
+      base[x] += add;
+    }
+    __syncthreads();
   }
 }
 
@@ -529,14 +779,61 @@ int decode_max_pairs() { return kMaxPairs; }
 int decode_max_experts() { return kMaxExperts; }
 
 namespace {
+
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsSizes {
+  size_t x32, h, y, offsets, perm, routed, ctl, arrive;
+};
+
+WsSizes ws_sizes(const pw_moe_shape& s) {
+  const size_t P = static_cast<size_t>(s.T) * s.k;
+  WsSizes z;
+  z.x32 = round256(4 * static_cast<size_t>(s.T) * s.H);
+  z.h = round256(4 * P * s.I);
+  z.y = round256(4 * P * s.H);
+  z.offsets = round256(4 * (static_cast<size_t>(s.E) + 1));
+  z.perm = round256(4 * P);
+  z.routed = round256(4 * static_cast<size_t>(s.E));
+  z.ctl = 256;
+  z.arrive = round256(4 * static_cast<size_t>(s.H / 32));
+  return z;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <typename Kernel>
+cudaError_t launch_dependent(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             const LayerArgs& a, const DecodeWs& w, const BitConsts& bc) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a, w, bc);
+}
+
 }  // namespace
 
-// Workspace: h [T*k][I] fp32 | y [T*k][H] fp32 | per-row-tile counters [H/32].
+// Workspace: x32 [T][H] | h [T*k][I] | y [T*k][H] fp32 | offsets [E+1] |
+// perm [T*k] | routed lists [E] x 2 | control words | arrival counters [H/32].
 size_t decode_workspace_bytes(const pw_moe_shape& s) {
-  const size_t pairs = static_cast<size_t>(s.T) * s.k;
-  return round256(sizeof(float) * pairs * s.I) + round256(sizeof(float) * pairs * s.H) +
-         round256(sizeof(int) * (s.H / 32));
+  const WsSizes z = ws_sizes(s);
+  return z.x32 + z.h + z.y + z.offsets + z.perm + 2 * z.routed + z.ctl + z.arrive;
 }
 
 cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream) {
@@ -553,20 +850,50 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream) {
   }
   const int n_pairs = a.T * a.k;
   if (n_pairs == 0) return cudaSuccess;
-  const int slots = min(a.E, n_pairs);
-  char* base = static_cast<char*>(ws);
-  float* h_ws = reinterpret_cast<float*>(base);
-  base += round256(sizeof(float) * static_cast<size_t>(n_pairs) * a.I);
-  float* y_ws = reinterpret_cast<float*>(base);
-  base += round256(sizeof(float) * static_cast<size_t>(n_pairs) * a.H);
-  int* tile_count = reinterpret_cast<int*>(base);
-  decode_gateup_kernel<<<dim3(a.I / kPairsPerTile, slots), kThreads, kSmemBytes, stream>>>(
-      a, h_ws, tile_count);
+  pw_moe_shape shape{a.T, a.H, a.I, a.E, a.k};
+  const WsSizes z = ws_sizes(shape);
+  char* p = static_cast<char*>(ws);
+  DecodeWs w;
+  w.x32 = reinterpret_cast<float*>(p); p += z.x32;
+  w.h = reinterpret_cast<float*>(p); p += z.h;
+  w.y = reinterpret_cast<float*>(p); p += z.y;
+  w.offsets = reinterpret_cast<int*>(p); p += z.offsets;
+  w.perm = reinterpret_cast<int*>(p); p += z.perm;
+  w.routed_gu = reinterpret_cast<int*>(p); p += z.routed;
+  w.routed_dn = reinterpret_cast<int*>(p); p += z.routed;
+  w.ctl = reinterpret_cast<int*>(p); p += z.ctl;
+  w.arrive = reinterpret_cast<int*>(p);
+
+  const size_t prep_smem = sizeof(int) * static_cast<size_t>(a.E) * (2 + kPrepWarps);
+  if (prep_smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(decode_prep_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(prep_smem));
+    if (e != cudaSuccess) return e;
+  }
+  const long long n4 = static_cast<long long>(a.T) * a.H / 4;
+  const long long conv = (n4 + kPrepThreads - 1) / kPrepThreads;
+  const int prep_grid = 1 + static_cast<int>(conv < 4 * 152 ? conv : 4 * 152);
+  decode_prep_kernel<<<prep_grid, kPrepThreads, prep_smem, stream>>>(a, w);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_down_kernel<<<dim3((a.H + kDownRows - 1) / kDownRows, slots), kThreads, kSmemBytes,
-                       stream>>>(a, h_ws, y_ws, tile_count);
-  return cudaGetLastError();
+
+  const int slots = a.E < n_pairs ? a.E : n_pairs;
+  const int resident = 2 * sm_count();
+  const int gu_tiles = slots * (a.I / kPairsPerTile);
+  const int dn_tiles = slots * ((a.H + kDownRows - 1) / kDownRows);
+  BitConsts bc;
+  bc.hi7 = 1u << 25;
+  bc.mul7 = (1u << 7) + 1u;
+  bc.hi14 = 1u << 18;
+  bc.mul14 = (1u << 14) + 1u;
+  bc.hi4 = 1u << 28;
+  bc.mul4 = 1u << 4;
+  e = launch_dependent(decode_gateup_kernel, dim3(gu_tiles < resident ? gu_tiles : resident),
+                       dim3(kThreads), kSmemBytes, stream, a, w, bc);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(decode_down_kernel, dim3(dn_tiles < resident ? dn_tiles : resident),
+                          dim3(kThreads), kSmemBytes, stream, a, w, bc);
 }
 
 }  // namespace pw

@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
+DECODE_LAUNCHES_PER_CALL = 3   # hidden -> fp32, gate_up + SiLU, down + combine
 HBM_FALLBACK_GBS = 6800.0
 KERNEL_SOURCES = ("any_precision_bitplane_gb300/csrc/pw_decode.cu",
                   "any_precision_bitplane_gb300/csrc/pw_prefill.cu")
@@ -436,11 +437,12 @@ def native(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "pw_moe_forward decode launch pair (gateup + down)",
+                     "kernel": "pw_moe_forward decode call (3 launches: hidden->fp32, "
+                               "gate_up+SiLU, down+combine)",
                      "bytes_per_launch": step_bytes,
                      "traffic": recorded_traffic(args.workload, T)},
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": DECODE_LAUNCHES_PER_CALL * args.steps,
         "clocks": clocks,
     }
     if sweep:

@@ -243,8 +243,9 @@ int32_t pw_prefill_min_pairs(const pw_moe_shape* shape);
  * workspace: the scratch lives in one static device array of 8 MiB inside
  * libpw (every GPU that loads the library keeps those 8 MiB until the process
  * exits).  The caller still passes inputs and outputs.
- *   - Shapes whose decode scratch, 4*T*k*(I + H) bytes plus 4*H/32 rounded
- *     up to 256-byte sections, exceeds 8 MiB are rejected with
+ *   - Shapes whose decode scratch, about 4*T*H + 4*T*k*(I + H + 1) + 12*E
+ *     + H/8 bytes (each section rounded up to 256 bytes), exceeds 8 MiB are
+ *     rejected with
  *     PW_ERR_WORKSPACE (use pw_moe_forward with a workspace instead), as
  *     are shapes beyond the decode path's limits (PW_ERR_SHAPE).
  *   - The first call on each device looks up the array's device address
