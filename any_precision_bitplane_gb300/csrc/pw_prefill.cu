@@ -8,23 +8,29 @@
 //
 //   permute    pairs grouped by expert (offsets, perm)          [pw_route.cu]
 //   gather     xg[pos] = fp16(hidden[perm[pos] / k])            (one pass)
-//   gate_up    per (expert, 64 gate/up row pairs, 256 tokens):  D = W_gu x^T
+//   gate_up    per (expert, 64 gate/up row pairs, 512 tokens):  D = W_gu x^T
 //              in TMEM, epilogue h = SiLU(g) * u -> fp16 h[pos]
-//   down       per (expert, 128 down rows, 256 tokens):         D = W_dn h^T,
+//   down       per (expert, 128 down rows, 512 tokens):         D = W_dn h^T,
 //              epilogue y[pair] (fp32)
 //   combine    out[t] = sum_j w_tj * y[t*k + j], j order        (one pass)
 //
-// GEMM kernel (one CTA per SM, persistent over a static tile list):
-//   warps 0-3  dequant producers, thread r owns A-tile row r: read the row's
-//              top-q plane words (one word column of 128 consecutive rows is
-//              contiguous, so these loads coalesce), rebuild each index, look it up in the row's
-//              LUT (shared memory) and write fp16 into the 128-byte-swizzled,
-//              K-major A stage; then the epilogue of the same rows from TMEM.
-//   warp 4     TMA producer for the token operand (fp16 rows, 128B swizzle).
-//   warp 5     allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=256,
-//              K=16, fp16 x fp16 -> fp32) and tcgen05.commit.
-// Stages are handed over with mbarriers; every wait is bounded and a timeout
-// latches PW_ERR_TIMEOUT and unwinds without trapping.
+// GEMM kernel (one CTA per SM, persistent over a static tile list; 14 warps):
+//   warps 0-7   dequant producers in two sets of four that take alternate
+//               k-steps; thread r of a set owns A-tile row r.  Per k-step (32
+//               columns) it loads one word of each of the row's top q planes
+//               (a word column of consecutive rows is contiguous), rebuilds
+//               the 32 indices with a byte transpose and an 8x8 bit-matrix
+//               transpose, looks them up in the row's LUT (fp16, shared
+//               memory; a byte permute forms each address) and writes the
+//               fp16 row into the 64-byte-swizzled, K-major A stage.
+//   warps 8-11  epilogue: drain the TMEM accumulator (lane quarter = warp%4).
+//   warp 12     TMA producer for the token operand (fp16 rows, 64B swizzle).
+//   warp 13     allocates all 512 TMEM columns; lane 0 issues per k-step two
+//               K=16 steps of two tcgen05.mma (M=128, N=256 each, fp16 x
+//               fp16 -> fp32) into columns [0,256) and [256,512).
+// A weight tile is dequantised once per 512 tokens.  Stages are handed over
+// with mbarriers; every wait is bounded and a timeout latches PW_ERR_TIMEOUT
+// and unwinds without trapping.
 //
 // Operand precision: the weights are exact fp16 LUT values; hidden states are
 // converted bf16 -> fp16 (exact for |x| in fp16's normal range, |x| < 65504);
@@ -37,34 +43,44 @@
 #include <climits>
 #include <mutex>
 
+#include "pw_bits.cuh"
 #include "pw_internal.cuh"
 
 namespace pw {
 namespace {
 
 constexpr int BM = 128;                 // A rows per tile (MMA M)
-constexpr int BN = 256;                 // tokens per tile (MMA N)
-constexpr int BK = 64;                  // K per stage: one 128-byte swizzle atom of fp16
+constexpr int BN = 512;                 // tokens per tile: two MMAs of N = 256
+constexpr int BNH = 256;                // tokens per MMA
+constexpr int BK = 32;                  // K per stage: one plane word column, 64-byte rows
 constexpr int NST = 3;                  // pipeline stages
-constexpr int kDqThreads = 128;         // warps 0-3
-constexpr int kThreads = kDqThreads + 64;
-constexpr uint32_t kAStage = BM * BK * 2;   // 16 KB
-constexpr uint32_t kBStage = BN * BK * 2;   // 32 KB
+constexpr int kDqThreads = 256;         // warps 0-7
+constexpr int kEpiWarp0 = 8;            // warps 8-11
+constexpr int kTmaWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kThreads = 14 * 32;
+constexpr uint32_t kAStage = BM * BK * 2;     // 8 KB
+constexpr uint32_t kBHalf = BNH * BK * 2;     // 16 KB per 256 tokens
+constexpr uint32_t kBStage = 2 * kBHalf;      // 32 KB
 constexpr uint32_t kLutBytes = 256 * BM * 2;  // fp16 [256][128]
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSpinLimit = 1u << 24;
 constexpr int kMaxExperts = 1024;
 
-// shared memory carve-up (offsets from the 1024-aligned base)
-constexpr uint32_t kOffA = 0;
+// Shared memory (offsets from the dynamic base, which must be 1024-aligned):
+// the LUT sits at offset 0 so that lookups address the dynamic symbol with a
+// register offset only.
+constexpr uint32_t kOffLut = 0;
+constexpr uint32_t kOffA = kOffLut + kLutBytes;
 constexpr uint32_t kOffB = kOffA + NST * kAStage;
-constexpr uint32_t kOffLut = kOffB + NST * kBStage;
-constexpr uint32_t kOffBar = kOffLut + kLutBytes;            // 8-byte barriers
+constexpr uint32_t kOffBar = kOffB + NST * kBStage;            // 8-byte barriers
 constexpr int kBarFullA = 0, kBarFullB = NST, kBarEmpty = 2 * NST, kBarAccFull = 3 * NST,
               kBarAccEmpty = 3 * NST + 1, kBarFinal = 3 * NST + 2, kNumBars = 3 * NST + 3;
-constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;        // tmem base, abort flag
-constexpr uint32_t kOffPrefix = kOffMisc + 16;               // tile prefix [E+1]
-constexpr size_t kSmemBytes = 1024 + kOffPrefix + 4 * (kMaxExperts + 1);
+constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;          // tmem base, abort flag
+constexpr uint32_t kOffPrefix = kOffMisc + 16;                 // tile prefix [E+1]
+constexpr size_t kSmemBytes = kOffPrefix + 4 * (kMaxExperts + 1);
+
+extern __shared__ __align__(1024) unsigned char g_psmem[];
 
 enum Mode { kGateUp = 0, kDown = 1 };
 
@@ -138,30 +154,31 @@ __device__ __forceinline__ void named_sync_dq() {
   asm volatile("bar.sync 1, %0;" ::"n"(kDqThreads) : "memory");
 }
 
-// K-major operand, 128-byte swizzle: rows of 128 bytes, 8-row atoms of 1024
+// K-major operand, 64-byte swizzle: rows of 64 bytes, 8-row atoms of 512
 // bytes (stride-dimension offset), leading-dimension offset unused (1).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>(1) << 16;
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(512 >> 4) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= static_cast<uint64_t>(4) << 61;
   return d;
 }
 
 // kind::f16 instruction descriptor: fp32 accumulator, fp16 A and B, both
-// K-major, N = BN, M = BM.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) |
-                            (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
+// K-major, M = BM, N = n (a multiple of 16, at most 256).
+__device__ __forceinline__ uint32_t make_idesc(int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+}
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(tmem_d), "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+      ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 
@@ -207,8 +224,7 @@ __device__ __forceinline__ int m_tiles(Mode mode, const GemmArgs& a) {
 }
 
 // Tile t of the list ordered (expert, row tile, token tile), token tile fastest.
-__device__ __forceinline__ Tile tile_at(int t, const int* prefix, int E, int mt,
-                                        const int32_t* offsets) {
+__device__ __forceinline__ Tile tile_at(int t, const int* prefix, int E, const int32_t* offsets) {
   int lo = 0, hi = E;  // find e with prefix[e] <= t < prefix[e+1]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -221,7 +237,6 @@ __device__ __forceinline__ Tile tile_at(int t, const int* prefix, int E, int mt,
   r.e = e;
   r.m = local / nt;
   r.n = local % nt;
-  (void)mt;
   return r;
 }
 
@@ -255,73 +270,78 @@ __device__ void report_unusable(Mode mode, const GemmArgs& a, int e) {
 
 // ---------------------------------------------------------------- dequant
 
-// Thread r: fill A-stage row r with the 64 weights of k-step s.
+// LUT of the tile's rows: byte v*256 + r*2 holds LUT_q[row(r)][v] (fp16).  The
+// 256 dequant threads split each row's entries in two halves.
 template <int Q>
-__device__ __forceinline__ void dequant_kstep(const uint32_t* row_planes, long long plane_stride,
-                                              long long N, int s, const uint16_t* lut_s, int r,
-                                              uint8_t* a_stage) {
-  uint32_t w[Q][2];
-#pragma unroll
-  for (int p = 0; p < Q; ++p) {
-    w[p][0] = __ldg(row_planes + p * plane_stride + (2 * s) * N);
-    w[p][1] = __ldg(row_planes + p * plane_stride + (2 * s + 1) * N);
-  }
-  const uint32_t row_base = (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint32_t packed[4];
-#pragma unroll
-    for (int j2 = 0; j2 < 4; ++j2) {
-      uint32_t pair = 0;
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int kk = c * 8 + j2 * 2 + jj;
-        const int word = kk >> 5, bit = kk & 31;
-        uint32_t idx = 0;
-#pragma unroll
-        for (int p = 0; p < Q; ++p) idx = (idx << 1) | ((w[p][word] >> bit) & 1u);
-        pair |= static_cast<uint32_t>(lut_s[idx * BM + r]) << (16 * jj);
-      }
-      packed[j2] = pair;
-    }
-    *reinterpret_cast<uint4*>(a_stage + row_base + ((c ^ (r & 7)) << 4)) =
-        make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  }
-}
-
-// LUT of the tile's rows: lut_s[v * 128 + r] = LUT_q[row(r)][v] (fp16 bits).
-template <int Q>
-__device__ __forceinline__ void load_lut(const uint16_t* lut, int grow, int r, uint16_t* lut_s) {
+__device__ __forceinline__ void load_lut(const uint16_t* lut, int grow, int r, int half) {
   constexpr int kEnt = 1 << Q;
+  constexpr int kVec = kEnt / 8;
   const uint4* src = reinterpret_cast<const uint4*>(lut + static_cast<long long>(grow) * kEnt);
 #pragma unroll 4
-  for (int vec = 0; vec < kEnt / 8; ++vec) {
+  for (int vec = half; vec < kVec; vec += 2) {
     const uint4 raw = __ldg(src + vec);
     const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) lut_s[(vec * 8 + j) * BM + r] = h[j];
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint16_t*>(g_psmem + kOffLut + (vec * 8 + j) * 256 + r * 2) = h[j];
+  }
+}
+
+// Thread r: fill A-stage row r with the 32 weights of k-step (word column) ks.
+template <int Q>
+__device__ __forceinline__ void dequant_kstep(const uint32_t* row_planes, long long plane_stride,
+                                              long long N, int ks, int r, uint32_t a_stage,
+                                              const BitConsts& bc) {
+  uint32_t w[Q];
+#pragma unroll
+  for (int p = 0; p < Q; ++p) w[p] = __ldg(row_planes + p * plane_stride + ks * N);
+  uint32_t ib[8];
+  planes_to_index_bytes<Q>(w, ib, bc);
+  const uint32_t rb = static_cast<uint32_t>(r) << 1;
+  const uint32_t row_base = a_stage + r * 64;
+  const uint32_t sw = (r >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {   // 16-byte chunk c = columns 8c .. 8c+7
+    uint32_t packed[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t word = ib[2 * c + h];
+      uint32_t v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t off = __byte_perm(word, rb, 0x6504 | (j << 4));
+        v[j] = *reinterpret_cast<const uint16_t*>(g_psmem + off);
+      }
+      packed[2 * h] = __byte_perm(v[0], v[1], 0x5410);
+      packed[2 * h + 1] = __byte_perm(v[2], v[3], 0x5410);
+    }
+    const uint32_t dst = row_base + ((c ^ sw) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[0]),
+                 "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
+                 : "memory");
   }
 }
 
 template <int Q>
 __device__ void dequant_tile(const GemmArgs& a, Mode mode, const pw_block_entry& ent, int m,
-                             int ksteps, int K, int r, uint8_t* smem, uint32_t bar_base,
-                             uint32_t& it, volatile int* abort) {
-  uint16_t* lut_s = reinterpret_cast<uint16_t*>(smem + kOffLut);
+                             int ksteps, uint32_t it_base, int set, int r, uint32_t bar_base,
+                             volatile int* abort, const BitConsts& bc) {
   const int grow = block_row(mode, a, m, r);
-  named_sync_dq();                      // every thread is done with the previous tile's LUT
-  if (!*abort) load_lut<Q>(ent.lut, grow, r, lut_s);
+  named_sync_dq();                      // both sets are done with the previous tile's LUT
+  if (!*abort) load_lut<Q>(ent.lut, grow, r, set);
   named_sync_dq();
-  const int KW = K / 32;
   const long long N = (mode == kGateUp) ? 2LL * a.I : a.H;
+  const long long KW = ((mode == kGateUp) ? a.H : a.I) / 32;
   const long long plane_stride = N * KW;
   const uint32_t* row_planes = ent.planes + grow;
-  for (int s = 0; s < ksteps; ++s, ++it) {
+  const uint32_t a_base = smem_u32(g_psmem) + kOffA;
+  for (int ks = set; ks < ksteps; ks += 2) {
+    const uint32_t it = it_base + ks;
     const int stage = it % NST;
     const uint32_t par = (it / NST) & 1u;
     if (*abort) continue;
     if (!mbar_wait(bar_base + 8 * (kBarEmpty + stage), par ^ 1u, abort, a.status)) continue;
-    dequant_kstep<Q>(row_planes, plane_stride, N, s, lut_s, r, smem + kOffA + stage * kAStage);
+    dequant_kstep<Q>(row_planes, plane_stride, N, ks, r, a_base + stage * kAStage, bc);
     fence_proxy_async();
     mbar_arrive(bar_base + 8 * (kBarFullA + stage));
   }
@@ -330,9 +350,9 @@ __device__ void dequant_tile(const GemmArgs& a, Mode mode, const pw_block_entry&
 // ---------------------------------------------------------------- epilogue
 
 __device__ void epilogue(const GemmArgs& a, Mode mode, const Tile& tile, int pos0, int ntok,
-                         bool usable, uint32_t tmem_base, int r, uint32_t bar_base,
+                         bool usable, uint32_t tmem_base, int quarter, int lane, uint32_t bar_base,
                          uint32_t acc_par, volatile int* abort) {
-  const int lane = r & 31, warp = r >> 5;
+  const int r = quarter * 32 + lane;
   if (usable) {
     if (*abort || !mbar_wait(bar_base + 8 * kBarAccFull, acc_par, abort, a.status)) return;
     tc_fence_after();
@@ -341,7 +361,7 @@ __device__ void epilogue(const GemmArgs& a, Mode mode, const Tile& tile, int pos
     if (c * 32 >= ntok) break;
     float v[32];
     if (usable) {
-      tmem_ld32(tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + c * 32, v);
+      tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = 0.f;
@@ -381,19 +401,22 @@ __device__ void epilogue(const GemmArgs& a, Mode mode, const Tile& tile, int pos
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    dq_gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmap_b) {
+    dq_gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmap_b,
+                   const BitConsts bc) {
   constexpr Mode mode = static_cast<Mode>(MODE);
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const uint32_t bar_base = smem_u32(smem + kOffBar);
-  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  const uint32_t sbase = smem_u32(g_psmem);
+  const uint32_t bar_base = sbase + kOffBar;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(g_psmem + kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(misc + 1);
-  int* prefix = reinterpret_cast<int*>(smem + kOffPrefix);
+  int* prefix = reinterpret_cast<int*>(g_psmem + kOffPrefix);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = m_tiles(mode, a);
   const int K = (mode == kGateUp) ? a.H : a.I;
   const int ksteps = K / BK;
+  if (sbase & 1023u) {   // the swizzled stages need a 1024-byte aligned base
+    if (tid == 0) latch_status(a.status, PW_ERR_CUDA);
+    return;
+  }
 
   if (tid == 0) {
     *abort = 0;
@@ -404,16 +427,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     prefix[a.E] = run;
     for (int i = 0; i < NST; ++i) {
-      mbar_init(bar_base + 8 * (kBarFullA + i), kDqThreads);
+      mbar_init(bar_base + 8 * (kBarFullA + i), kDqThreads / 2);
       mbar_init(bar_base + 8 * (kBarFullB + i), 1);
       mbar_init(bar_base + 8 * (kBarEmpty + i), 1);
     }
     mbar_init(bar_base + 8 * kBarAccFull, 1);
-    mbar_init(bar_base + 8 * kBarAccEmpty, kDqThreads);
+    mbar_init(bar_base + 8 * kBarAccEmpty, 128);
     mbar_init(bar_base + 8 * kBarFinal, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(misc)),
                  "r"(kTmemCols)
@@ -426,44 +449,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = misc[0];
   const int total = prefix[a.E];
 
-  if (warp < 4) {
-    // ---- dequant producers + epilogue
-    uint32_t it = 0, acc_it = 0;
+  if (warp < 8) {
+    // ---- dequant producers: set 0 = warps 0-3 (even k-steps), set 1 = warps 4-7
+    const int set = warp >> 2, r = tid & 127;
+    uint32_t it_base = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tile = tile_at(t, prefix, a.E, mt, a.offsets);
+      const Tile tile = tile_at(t, prefix, a.E, a.offsets);
+      const bool usable = tile_usable(mode, a, tile.e);
+      if (!usable) continue;
+      const pw_block_entry ent = a.table[2 * tile.e + (mode == kGateUp ? 0 : 1)];
+      switch (ent.q) {
+        case 3: dequant_tile<3>(a, mode, ent, tile.m, ksteps, it_base, set, r, bar_base, abort, bc); break;
+        case 4: dequant_tile<4>(a, mode, ent, tile.m, ksteps, it_base, set, r, bar_base, abort, bc); break;
+        case 5: dequant_tile<5>(a, mode, ent, tile.m, ksteps, it_base, set, r, bar_base, abort, bc); break;
+        case 6: dequant_tile<6>(a, mode, ent, tile.m, ksteps, it_base, set, r, bar_base, abort, bc); break;
+        default: dequant_tile<8>(a, mode, ent, tile.m, ksteps, it_base, set, r, bar_base, abort, bc); break;
+      }
+      it_base += ksteps;
+    }
+  } else if (warp < kTmaWarp) {
+    // ---- epilogue
+    const int quarter = warp - kEpiWarp0;
+    uint32_t acc_it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tile = tile_at(t, prefix, a.E, a.offsets);
       const int pos0 = a.offsets[tile.e] + tile.n * BN;
       const int ntok = min(BN, a.offsets[tile.e + 1] - pos0);
       const bool usable = tile_usable(mode, a, tile.e);
-      if (!usable && tid == 0) report_unusable(mode, a, tile.e);
-      if (usable) {
-        const pw_block_entry ent = a.table[2 * tile.e + (mode == kGateUp ? 0 : 1)];
-        switch (ent.q) {
-          case 3: dequant_tile<3>(a, mode, ent, tile.m, ksteps, K, tid, smem, bar_base, it, abort); break;
-          case 4: dequant_tile<4>(a, mode, ent, tile.m, ksteps, K, tid, smem, bar_base, it, abort); break;
-          case 5: dequant_tile<5>(a, mode, ent, tile.m, ksteps, K, tid, smem, bar_base, it, abort); break;
-          case 6: dequant_tile<6>(a, mode, ent, tile.m, ksteps, K, tid, smem, bar_base, it, abort); break;
-          default: dequant_tile<8>(a, mode, ent, tile.m, ksteps, K, tid, smem, bar_base, it, abort); break;
-        }
-      }
-      epilogue(a, mode, tile, pos0, ntok, usable, tmem_base, tid, bar_base, acc_it & 1u, abort);
+      if (!usable && quarter == 0 && lane == 0) report_unusable(mode, a, tile.e);
+      epilogue(a, mode, tile, pos0, ntok, usable, tmem_base, quarter, lane, bar_base, acc_it & 1u,
+               abort);
       if (usable) ++acc_it;
     }
-  } else if (warp == 4) {
+  } else if (warp == kTmaWarp) {
     // ---- TMA producer for the token operand
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
       uint32_t it = 0;
       for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
-        const Tile tile = tile_at(t, prefix, a.E, mt, a.offsets);
+        const Tile tile = tile_at(t, prefix, a.E, a.offsets);
         if (!tile_usable(mode, a, tile.e)) continue;
         const int pos0 = a.offsets[tile.e] + tile.n * BN;
+        const int ntok = min(BN, a.offsets[tile.e + 1] - pos0);
+        const int halves = ntok > BNH ? 2 : 1;
         for (int s = 0; s < ksteps; ++s, ++it) {
           const int stage = it % NST;
           const uint32_t par = (it / NST) & 1u;
           if (!mbar_wait(bar_base + 8 * (kBarEmpty + stage), par ^ 1u, abort, a.status)) break;
           const uint32_t full = bar_base + 8 * (kBarFullB + stage);
-          mbar_arrive_tx(full, kBStage);
-          tma_load_2d(smem_u32(smem + kOffB + stage * kBStage), &tmap_b, s * BK, pos0, full);
+          mbar_arrive_tx(full, halves * kBHalf);
+          for (int h = 0; h < halves; ++h)
+            tma_load_2d(sbase + kOffB + stage * kBStage + h * kBHalf, &tmap_b, s * BK,
+                        pos0 + h * BNH, full);
         }
       }
       if (*abort) {
@@ -481,8 +518,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, acc_it = 0;
       bool issued = false;
       for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
-        const Tile tile = tile_at(t, prefix, a.E, mt, a.offsets);
+        const Tile tile = tile_at(t, prefix, a.E, a.offsets);
         if (!tile_usable(mode, a, tile.e)) continue;
+        const int pos0 = a.offsets[tile.e] + tile.n * BN;
+        const int ntok = min(BN, a.offsets[tile.e + 1] - pos0);
+        const int n0 = min(BNH, (ntok + 15) & ~15);
+        const int n1 = ntok > BNH ? ((ntok - BNH + 15) & ~15) : 0;
+        const uint32_t id0 = make_idesc(n0), id1 = make_idesc(n1 > 0 ? n1 : 16);
         if (!mbar_wait(bar_base + 8 * kBarAccEmpty, (acc_it & 1u) ^ 1u, abort, a.status)) break;
         tc_fence_after();
         for (int s = 0; s < ksteps; ++s, ++it) {
@@ -491,12 +533,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar_base + 8 * (kBarFullA + stage), par, abort, a.status)) break;
           if (!mbar_wait(bar_base + 8 * (kBarFullB + stage), par, abort, a.status)) break;
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + kOffA + stage * kAStage);
-          const uint32_t b_addr = smem_u32(smem + kOffB + stage * kBStage);
+          const uint32_t a_addr = sbase + kOffA + stage * kAStage;
+          const uint32_t b_addr = sbase + kOffB + stage * kBStage;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_f16(tmem_base, smem_desc(a_addr + kk * 32), smem_desc(b_addr + kk * 32),
-                    (s > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+            mma_f16(tmem_base, smem_desc(a_addr + kk * 32), smem_desc(b_addr + kk * 32), id0, acc);
+            if (n1 > 0)
+              mma_f16(tmem_base + BNH, smem_desc(a_addr + kk * 32),
+                      smem_desc(b_addr + kBHalf + kk * 32), id1, acc);
+          }
           issued = true;
           mma_commit(bar_base + 8 * (kBarEmpty + stage));
         }
@@ -514,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(kTmemCols)
@@ -615,16 +661,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D fp16 [rows][cols] row-major, box {BK cols, BN rows}, 128-byte swizzle.
+// 2D fp16 [rows][cols] row-major, box {BK cols, BNH rows}, 64-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, int rows, int cols) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {BK, BN};
+  cuuint32_t box[2] = {BK, BNH};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -695,9 +741,10 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   g.y_ws = w.y;
   g.status = la.status;
   const int grid = num_sms();
-  dq_gemm_kernel<kGateUp><<<grid, kThreads, kSmemBytes, stream>>>(g, map_x);
+  const BitConsts bc = make_bit_consts();
+  dq_gemm_kernel<kGateUp><<<grid, kThreads, kSmemBytes, stream>>>(g, map_x, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  dq_gemm_kernel<kDown><<<grid, kThreads, kSmemBytes, stream>>>(g, map_h);
+  dq_gemm_kernel<kDown><<<grid, kThreads, kSmemBytes, stream>>>(g, map_h, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long cwork = static_cast<long long>(la.T) * la.H;
   const int cblocks = static_cast<int>(std::min<long long>((cwork + 255) / 256, 152LL * 32));
