@@ -270,8 +270,15 @@ __device__ void report_unusable(Mode mode, const GemmArgs& a, int e) {
 
 // ---------------------------------------------------------------- dequant
 
-// LUT of the tile's rows: byte v*256 + r*2 holds LUT_q[row(r)][v] (fp16).  The
-// 256 dequant threads split each row's entries in two halves.
+// Byte offset of row r's entries inside a LUT line: rows r and r+64 share
+// one 4-byte word, so the 32 consecutive rows of a warp use 32 different
+// banks.  Fits in one byte (at most 254).
+__device__ __forceinline__ uint32_t lut_row_bytes(int r) {
+  return (static_cast<uint32_t>(r & 63) << 2) | (static_cast<uint32_t>(r >> 6) << 1);
+}
+
+// LUT of the tile's rows: byte v*256 + lut_row_bytes(r) holds LUT_q[row(r)][v]
+// (fp16).  The 256 dequant threads split each row's entries in two halves.
 template <int Q>
 __device__ __forceinline__ void load_lut(const uint16_t* lut, int grow, int r, int half) {
   constexpr int kEnt = 1 << Q;
@@ -283,21 +290,25 @@ __device__ __forceinline__ void load_lut(const uint16_t* lut, int grow, int r, i
     const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<uint16_t*>(g_psmem + kOffLut + (vec * 8 + j) * 256 + r * 2) = h[j];
+      *reinterpret_cast<uint16_t*>(g_psmem + kOffLut + (vec * 8 + j) * 256 + lut_row_bytes(r)) =
+          h[j];
   }
 }
 
-// Thread r: fill A-stage row r with the 32 weights of k-step (word column) ks.
 template <int Q>
-__device__ __forceinline__ void dequant_kstep(const uint32_t* row_planes, long long plane_stride,
-                                              long long N, int ks, int r, uint32_t a_stage,
-                                              const BitConsts& bc) {
-  uint32_t w[Q];
+__device__ __forceinline__ void load_words(const uint32_t* row_planes, long long plane_stride,
+                                           long long N, int ks, uint32_t (&w)[Q]) {
 #pragma unroll
   for (int p = 0; p < Q; ++p) w[p] = __ldg(row_planes + p * plane_stride + ks * N);
+}
+
+// Thread r: fill A-stage row r with the 32 weights whose plane words are w.
+template <int Q>
+__device__ __forceinline__ void dequant_kstep(const uint32_t (&w)[Q], int r, uint32_t a_stage,
+                                              const BitConsts& bc) {
   uint32_t ib[8];
   planes_to_index_bytes<Q>(w, ib, bc);
-  const uint32_t rb = static_cast<uint32_t>(r) << 1;
+  const uint32_t rb = lut_row_bytes(r);
   const uint32_t row_base = a_stage + r * 64;
   const uint32_t sw = (r >> 1) & 3;
 #pragma unroll
@@ -335,13 +346,24 @@ __device__ void dequant_tile(const GemmArgs& a, Mode mode, const pw_block_entry&
   const long long plane_stride = N * KW;
   const uint32_t* row_planes = ent.planes + grow;
   const uint32_t a_base = smem_u32(g_psmem) + kOffA;
+  // plane words are loaded two k-steps (of this set) ahead
+  uint32_t n1[Q], n2[Q];
+  if (set < ksteps) load_words<Q>(row_planes, plane_stride, N, set, n1);
+  if (set + 2 < ksteps) load_words<Q>(row_planes, plane_stride, N, set + 2, n2);
   for (int ks = set; ks < ksteps; ks += 2) {
+    uint32_t cur[Q];
+#pragma unroll
+    for (int p = 0; p < Q; ++p) {
+      cur[p] = n1[p];
+      n1[p] = n2[p];
+    }
+    if (ks + 4 < ksteps) load_words<Q>(row_planes, plane_stride, N, ks + 4, n2);
     const uint32_t it = it_base + ks;
     const int stage = it % NST;
     const uint32_t par = (it / NST) & 1u;
     if (*abort) continue;
     if (!mbar_wait(bar_base + 8 * (kBarEmpty + stage), par ^ 1u, abort, a.status)) continue;
-    dequant_kstep<Q>(row_planes, plane_stride, N, ks, r, a_base + stage * kAStage, bc);
+    dequant_kstep<Q>(cur, r, a_base + stage * kAStage, bc);
     fence_proxy_async();
     mbar_arrive(bar_base + 8 * (kBarFullA + stage));
   }

@@ -52,6 +52,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--copies", type=int, default=0,
                     help="layer copies to rotate (0: enough to exceed 2x L2)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the prefill section and print its JSON")
+    ap.add_argument("--prefill-tokens", type=int, default=0,
+                    help="tokens of the prefill section (0: the workload's 4096)")
     return ap.parse_args()
 
 
@@ -292,14 +296,14 @@ def cpu_baseline(name, T, budget_s=20.0):
                       "blocks encoded before timing)" % (calls, T)}
 
 
-def prefill_section(pw, device, steps=5, warmup=2):
+def prefill_section(pw, device, steps=5, warmup=2, tokens=0):
     """Mixtral-shaped prefill (4096 tokens, top-2 of 8 experts, H=4096,
     I=14336): the dequantise-to-shared-memory tcgen05 path."""
     import torch
     from any_precision_bitplane_gb300.layer import DeviceLayer
     from workloads import configs, gen
     cfg = configs.config_by_name("mixtral_prefill")
-    T = cfg.T[0]
+    T = tokens if tokens > 0 else cfg.T[0]
     layer = gen.make_layer(cfg, 0)
     dl = DeviceLayer(layer, device=device)
     tok = gen.make_tokens(layer, T)
@@ -339,6 +343,13 @@ def native(args):
     import torch
     import any_precision_bitplane_gb300 as pw
     rank, world, local = dist_env()
+    if args.prefill_only:
+        torch.cuda.set_device(local)
+        pw.lib()
+        print(json.dumps(prefill_section(pw, torch.device("cuda", local), steps=args.steps,
+                                         warmup=args.warmup, tokens=args.prefill_tokens)),
+              flush=True)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
