@@ -14,23 +14,38 @@
 //              epilogue y[pair] (fp32)
 //   combine    out[t] = sum_j w_tj * y[t*k + j], j order        (one pass)
 //
-// GEMM kernel (one CTA per SM, persistent over a static tile list; 14 warps):
-//   warps 0-7   dequant producers in two sets of four that take alternate
-//               k-steps; thread r of a set owns A-tile row r.  Per k-step (32
-//               columns) it loads one word of each of the row's top q planes
-//               (a word column of consecutive rows is contiguous), rebuilds
-//               the 32 indices with a byte transpose and an 8x8 bit-matrix
-//               transpose, looks them up in the row's LUT (fp16, shared
-//               memory; a byte permute forms each address) and writes the
-//               fp16 row into the 64-byte-swizzled, K-major A stage.
-//   warps 8-11  epilogue: drain the TMEM accumulator (lane quarter = warp%4).
-//   warp 12     TMA producer for the token operand (fp16 rows, 64B swizzle).
-//   warp 13     allocates all 512 TMEM columns; lane 0 issues per k-step two
+// GEMM kernel: one CTA per SM, persistent, 23 warps in five roles.
+//   warp 20     scheduler and token-operand producer: takes tile ids from a
+//               global counter (SMs that draw cheap tiles take more of them),
+//               publishes each through a 4-deep ring in shared memory, and
+//               TMA-loads the fp16 token rows (64-byte swizzle) of every k-step.
+//   warp 21     plane producer: per k-step (32 columns = one plane word
+//               column), bulk-copies the words of the tile's 128 rows from
+//               each of the top q planes into a 6-deep ring (a word column of
+//               consecutive rows is contiguous: two 256-byte runs for a
+//               gate_up tile, one 512-byte run for a down tile), one copy
+//               per lane so that the copies of a k-step start together.
+//   warps 0-15  dequant: two sets of eight that take alternate k-steps.  In a
+//               set, four warps own columns 0-15 of the k-step and four own
+//               columns 16-31; each thread owns one A row.  A thread reads
+//               its row's q plane words from the ring, rebuilds 16 indices
+//               with a byte transpose and an 8x8 bit-matrix transpose, looks
+//               them up in the row's LUT (fp16, shared memory, every lane of
+//               a warp on its own bank) and writes 32 bytes of the
+//               64-byte-swizzled, K-major A stage.
+//   warp 22     allocates the 512 TMEM columns; lane 0 issues per k-step two
 //               K=16 steps of two tcgen05.mma (M=128, N=256 each, fp16 x
 //               fp16 -> fp32) into columns [0,256) and [256,512).
+//   warps 16-19 epilogue (TMEM lane quarter = warp % 4).  gate_up: gate and up
+//               rows of one h column sit 8 lanes apart, so one lane exchange
+//               pairs them; h = SiLU(g) * u (fp16) is staged in shared memory
+//               and written out as 128-byte rows.  down: y rows (fp32) go
+//               straight to each pair's output row.
 // A weight tile is dequantised once per 512 tokens.  Stages are handed over
-// with mbarriers; every wait is bounded and a timeout latches PW_ERR_TIMEOUT
-// and unwinds without trapping.
+// with mbarriers; every wait is bounded, and a timeout latches PW_ERR_TIMEOUT
+// and unwinds without trapping.  Decisions that named barriers depend on are
+// taken by one thread and shared through shared memory, so every thread of a
+// barrier group takes the same path even while unwinding.
 //
 // Operand precision: the weights are exact fp16 LUT values; hidden states are
 // converted bf16 -> fp16 (exact for |x| in fp16's normal range, |x| < 65504);
@@ -53,16 +68,24 @@ constexpr int BM = 128;                 // A rows per tile (MMA M)
 constexpr int BN = 512;                 // tokens per tile: two MMAs of N = 256
 constexpr int BNH = 256;                // tokens per MMA
 constexpr int BK = 32;                  // K per stage: one plane word column, 64-byte rows
-constexpr int NST = 3;                  // pipeline stages
-constexpr int kDqThreads = 256;         // warps 0-7
-constexpr int kEpiWarp0 = 8;            // warps 8-11
-constexpr int kTmaWarp = 12;
-constexpr int kMmaWarp = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int NST = 3;                  // A/B pipeline stages
+constexpr int NPS = 6;                  // plane-word stages
+constexpr int kDqWarps = 16;            // warps 0-15
+constexpr int kDqThreads = kDqWarps * 32;
+constexpr int kSetThreads = kDqThreads / 2;
+constexpr int kEpiWarp0 = 16;           // warps 16-19
+constexpr int kSchedWarp = 20;
+constexpr int kPlaneWarp = 21;
+constexpr int kMmaWarp = 22;
+constexpr int kThreads = 23 * 32;
+constexpr int kTileRing = 4;
+constexpr int kTileConsumers = 4;       // dequant, epilogue, plane producer, MMA issuer
 constexpr uint32_t kAStage = BM * BK * 2;     // 8 KB
 constexpr uint32_t kBHalf = BNH * BK * 2;     // 16 KB per 256 tokens
 constexpr uint32_t kBStage = 2 * kBHalf;      // 32 KB
+constexpr uint32_t kPlaneStage = 8 * BM * 4;  // up to 8 planes x 128 words
 constexpr uint32_t kLutBytes = 256 * BM * 2;  // fp16 [256][128]
+constexpr uint32_t kStageBuf = 32 * 64 * 2;   // epilogue: 32 tokens x 64 h columns, fp16
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSpinLimit = 1u << 24;
 constexpr int kMaxExperts = 1024;
@@ -73,12 +96,21 @@ constexpr int kMaxExperts = 1024;
 constexpr uint32_t kOffLut = 0;
 constexpr uint32_t kOffA = kOffLut + kLutBytes;
 constexpr uint32_t kOffB = kOffA + NST * kAStage;
-constexpr uint32_t kOffBar = kOffB + NST * kBStage;            // 8-byte barriers
-constexpr int kBarFullA = 0, kBarFullB = NST, kBarEmpty = 2 * NST, kBarAccFull = 3 * NST,
-              kBarAccEmpty = 3 * NST + 1, kBarFinal = 3 * NST + 2, kNumBars = 3 * NST + 3;
-constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;          // tmem base, abort flag
-constexpr uint32_t kOffPrefix = kOffMisc + 16;                 // tile prefix [E+1]
+constexpr uint32_t kOffPlanes = kOffB + NST * kBStage;
+constexpr uint32_t kOffStage = kOffPlanes + NPS * kPlaneStage;
+constexpr uint32_t kOffBar = kOffStage + 2 * kStageBuf;        // 8-byte barriers
+constexpr int kBarFullA = 0, kBarFullB = NST, kBarEmpty = 2 * NST, kBarPlFull = 3 * NST,
+              kBarPlEmpty = 3 * NST + NPS, kBarTileFull = 3 * NST + 2 * NPS,
+              kBarTileEmpty = kBarTileFull + kTileRing, kBarAccFull = kBarTileEmpty + kTileRing,
+              kBarAccEmpty = kBarAccFull + 1, kBarFinal = kBarAccEmpty + 1,
+              kNumBars = kBarFinal + 1;
+// misc words: [0] TMEM base, [1] abort flag, [2..5] tile ring, [6..7] dequant
+// tile slots, [8..9] epilogue tile slots, [10] epilogue accumulator flag
+constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;
+constexpr uint32_t kOffPrefix = kOffMisc + 64;                 // tile prefix [E+1]
 constexpr size_t kSmemBytes = kOffPrefix + 4 * (kMaxExperts + 1);
+static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
+static_assert(kOffB % 1024 == 0 && kOffA % 1024 == 0, "swizzled stages need 1024-byte alignment");
 
 extern __shared__ __align__(1024) unsigned char g_psmem[];
 
@@ -91,6 +123,7 @@ struct GemmArgs {
   const int32_t* perm;      // [n_pairs]
   __half* h_ws;             // [n_pairs][I] (gate_up writes, down reads through TMA)
   float* y_ws;              // [n_pairs][H]
+  int32_t* tile_counter;    // zeroed by the gather launch
   int32_t* status;
 };
 
@@ -213,6 +246,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void named_sync_epi() {
+  asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// Wait for the completion of every phase of barriers [first, first + n) that
+// the calling thread armed in its last `count` sequence numbers (so that
+// copies still in flight land before the CTA unwinds).
+__device__ void drain_copies(uint32_t bar_base, int first, int n, uint32_t seq_end,
+                             uint32_t count) {
+  for (uint32_t j = (seq_end > count ? seq_end - count : 0); j < seq_end; ++j) {
+    const uint32_t bar = bar_base + 8 * (first + j % n);
+    for (uint32_t i = 0; i < kSpinLimit && !mbar_try(bar, (j / n) & 1u); ++i) {
+    }
+  }
+}
+
 // ---------------------------------------------------------------- tile list
 
 struct Tile {
@@ -223,7 +285,9 @@ __device__ __forceinline__ int m_tiles(Mode mode, const GemmArgs& a) {
   return mode == kGateUp ? a.I / 64 : a.H / BM;
 }
 
-// Tile t of the list ordered (expert, row tile, token tile), token tile fastest.
+// Tile t of the list ordered (expert, row tile, token tile), token tile
+// fastest (the token tiles of one weight tile run side by side, so the
+// second read of its planes is an L2 hit).
 __device__ __forceinline__ Tile tile_at(int t, const int* prefix, int E, const int32_t* offsets) {
   int lo = 0, hi = E;  // find e with prefix[e] <= t < prefix[e+1]
   while (hi - lo > 1) {
@@ -238,14 +302,6 @@ __device__ __forceinline__ Tile tile_at(int t, const int* prefix, int E, const i
   r.m = local / nt;
   r.n = local % nt;
   return r;
-}
-
-// Row of the block behind A-tile row r.  gate_up tiles interleave gate and up
-// rows (even r: gate row, odd r: the matching up row) so that the epilogue
-// pairs them with one lane exchange.
-__device__ __forceinline__ int block_row(Mode mode, const GemmArgs& a, int m, int r) {
-  if (mode == kGateUp) return (r & 1) ? a.I + m * 64 + (r >> 1) : m * 64 + (r >> 1);
-  return m * BM + r;
 }
 
 __device__ __forceinline__ bool tile_usable(Mode mode, const GemmArgs& a, int e) {
@@ -268,117 +324,203 @@ __device__ void report_unusable(Mode mode, const GemmArgs& a, int e) {
     latch_status(a.status, PW_ERR_UNSUPPORTED_Q);
 }
 
+// One consumer's next tile id from the scheduler's ring (single thread).
+// INT_MAX once the CTA is unwinding.
+__device__ __forceinline__ int ring_take(uint32_t bar_base, const volatile int* ring, uint32_t& seq,
+                                         volatile int* abort, int32_t* status) {
+  const uint32_t slot = seq % kTileRing, par = (seq / kTileRing) & 1u;
+  ++seq;
+  if (!mbar_wait(bar_base + 8 * (kBarTileFull + slot), par, abort, status)) return INT_MAX;
+  const int t = ring[slot];
+  mbar_arrive(bar_base + 8 * (kBarTileEmpty + slot));
+  return t;
+}
+
 // ---------------------------------------------------------------- dequant
 
-// Byte offset of row r's entries inside a LUT line: rows r and r+64 share
-// one 4-byte word, so the 32 consecutive rows of a warp use 32 different
-// banks.  Fits in one byte (at most 254).
-__device__ __forceinline__ uint32_t lut_row_bytes(int r) {
-  return (static_cast<uint32_t>(r & 63) << 2) | (static_cast<uint32_t>(r >> 6) << 1);
+// Which A row, plane word and LUT slot a dequant thread owns.  Thread (w, L)
+// (w = warp % 4, L = lane) reads word `word` of each plane in the stage, so a
+// warp's reads are 32 consecutive words; its LUT slot puts lane L on bank L.
+//   gate_up: A rows come in groups of 16: 8 gate rows, then the 8 up rows of
+//            the same h columns; seg (0 gate, 1 up) = w / 2 and h column
+//            hc = 32 (w % 2) + L of the tile's 64.
+//   down:    A row 32 w + L.
+struct DqRow {
+  int r;          // A row (TMEM lane)
+  int word;       // word index in a plane's 128-word stage slab
+  int grow;       // row of the block
+  uint32_t slot;  // byte offset of the row's entries in a 256-byte LUT line
+};
+
+__device__ __forceinline__ DqRow dq_row(Mode mode, const GemmArgs& a, int m, int w, int lane) {
+  DqRow d;
+  d.slot = static_cast<uint32_t>((w >> 1) * 128 + lane * 4 + (w & 1) * 2);
+  if (mode == kGateUp) {
+    const int seg = w >> 1, hc = 32 * (w & 1) + lane;
+    d.word = seg * 64 + hc;
+    d.r = 16 * (hc >> 3) + 8 * seg + (hc & 7);
+    d.grow = seg * a.I + m * 64 + hc;
+  } else {
+    d.r = 32 * w + lane;
+    d.word = d.r;
+    d.grow = m * BM + d.r;
+  }
+  return d;
 }
 
-// LUT of the tile's rows: byte v*256 + lut_row_bytes(r) holds LUT_q[row(r)][v]
-// (fp16).  The 256 dequant threads split each row's entries in two halves.
+// The row's LUT into its slot: entry v at byte v*256 + slot (fp16).  The four
+// threads that own a row (two sets x two column halves) each move a quarter.
 template <int Q>
-__device__ __forceinline__ void load_lut(const uint16_t* lut, int grow, int r, int half) {
+__device__ __forceinline__ void load_lut(const uint16_t* lut, int grow, uint32_t slot, int part) {
   constexpr int kEnt = 1 << Q;
   constexpr int kVec = kEnt / 8;
+  constexpr int kPer = (kVec + 3) / 4;
   const uint4* src = reinterpret_cast<const uint4*>(lut + static_cast<long long>(grow) * kEnt);
-#pragma unroll 4
-  for (int vec = half; vec < kVec; vec += 2) {
-    const uint4 raw = __ldg(src + vec);
-    const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
+  uint4 raw[kPer];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<uint16_t*>(g_psmem + kOffLut + (vec * 8 + j) * 256 + lut_row_bytes(r)) =
-          h[j];
-  }
-}
-
-template <int Q>
-__device__ __forceinline__ void load_words(const uint32_t* row_planes, long long plane_stride,
-                                           long long N, int ks, uint32_t (&w)[Q]) {
+  for (int i = 0; i < kPer; ++i)
+    if (part + 4 * i < kVec) raw[i] = __ldg(src + part + 4 * i);
 #pragma unroll
-  for (int p = 0; p < Q; ++p) w[p] = __ldg(row_planes + p * plane_stride + ks * N);
-}
-
-// Thread r: fill A-stage row r with the 32 weights whose plane words are w.
-template <int Q>
-__device__ __forceinline__ void dequant_kstep(const uint32_t (&w)[Q], int r, uint32_t a_stage,
-                                              const BitConsts& bc) {
-  uint32_t ib[8];
-  planes_to_index_bytes<Q>(w, ib, bc);
-  const uint32_t rb = lut_row_bytes(r);
-  const uint32_t row_base = a_stage + r * 64;
-  const uint32_t sw = (r >> 1) & 3;
+  for (int i = 0; i < kPer; ++i) {
+    const int vec = part + 4 * i;
+    if (vec < kVec) {
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw[i]);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {   // 16-byte chunk c = columns 8c .. 8c+7
-    uint32_t packed[4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t word = ib[2 * c + h];
-      uint32_t v[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t off = __byte_perm(word, rb, 0x6504 | (j << 4));
-        v[j] = *reinterpret_cast<const uint16_t*>(g_psmem + off);
-      }
-      packed[2 * h] = __byte_perm(v[0], v[1], 0x5410);
-      packed[2 * h + 1] = __byte_perm(v[2], v[3], 0x5410);
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint16_t*>(g_psmem + kOffLut + (vec * 8 + j) * 256 + slot) = h[j];
     }
-    const uint32_t dst = row_base + ((c ^ sw) << 4);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[0]),
-                 "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
-                 : "memory");
   }
 }
 
+// Q plane words (P[0] = most significant plane) -> the indices of 16 of the
+// word's 32 columns, one per byte: `sel` picks bytes 0-1 (columns 0-15) or
+// bytes 2-3 (columns 16-31).  Byte j of ib[m] is the index of column 4m + j
+// of that half.
 template <int Q>
-__device__ void dequant_tile(const GemmArgs& a, Mode mode, const pw_block_entry& ent, int m,
-                             int ksteps, uint32_t it_base, int set, int r, uint32_t bar_base,
-                             volatile int* abort, const BitConsts& bc) {
-  const int grow = block_row(mode, a, m, r);
-  named_sync_dq();                      // both sets are done with the previous tile's LUT
-  if (!*abort) load_lut<Q>(ent.lut, grow, r, set);
-  named_sync_dq();
-  const long long N = (mode == kGateUp) ? 2LL * a.I : a.H;
-  const long long KW = ((mode == kGateUp) ? a.H : a.I) / 32;
-  const long long plane_stride = N * KW;
-  const uint32_t* row_planes = ent.planes + grow;
-  const uint32_t a_base = smem_u32(g_psmem) + kOffA;
-  // plane words are loaded two k-steps (of this set) ahead
-  uint32_t n1[Q], n2[Q];
-  if (set < ksteps) load_words<Q>(row_planes, plane_stride, N, set, n1);
-  if (set + 2 < ksteps) load_words<Q>(row_planes, plane_stride, N, set + 2, n2);
+__device__ __forceinline__ void planes_to_index_half(const uint32_t (&P)[Q], uint32_t sel,
+                                                     uint32_t (&ib)[4], const BitConsts& bc) {
+  uint32_t rr[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) rr[i] = (i < Q) ? P[Q - 1 - i] : 0u;
+  const uint32_t t0 = __byte_perm(rr[0], rr[1], sel), t2 = __byte_perm(rr[2], rr[3], sel);
+  const uint32_t t4 = __byte_perm(rr[4], rr[5], sel), t6 = __byte_perm(rr[6], rr[7], sel);
+  uint32_t lo0 = __byte_perm(t0, t2, 0x5410), hi0 = __byte_perm(t4, t6, 0x5410);
+  uint32_t lo1 = __byte_perm(t0, t2, 0x7632), hi1 = __byte_perm(t4, t6, 0x7632);
+  bit_transpose8(lo0, hi0, bc);
+  bit_transpose8(lo1, hi1, bc);
+  ib[0] = lo0;
+  ib[1] = hi0;
+  ib[2] = lo1;
+  ib[3] = hi1;
+}
+
+// This thread's share of a tile's k-steps: set `set` takes k-steps set,
+// set + 2, ...; `half` picks the 16 columns.
+template <int Q>
+__device__ void dequant_ksteps(const GemmArgs& a, const DqRow& d, int ksteps, uint32_t it_base,
+                               int set, int half, uint32_t sbase, uint32_t bar_base,
+                               volatile int* abort, const BitConsts& bc) {
+  const uint32_t sel = half ? 0x7362u : 0x5140u;
+  const uint32_t sw = (static_cast<uint32_t>(d.r) >> 1) & 3u;
   for (int ks = set; ks < ksteps; ks += 2) {
-    uint32_t cur[Q];
-#pragma unroll
-    for (int p = 0; p < Q; ++p) {
-      cur[p] = n1[p];
-      n1[p] = n2[p];
-    }
-    if (ks + 4 < ksteps) load_words<Q>(row_planes, plane_stride, N, ks + 4, n2);
     const uint32_t it = it_base + ks;
-    const int stage = it % NST;
-    const uint32_t par = (it / NST) & 1u;
-    if (*abort) continue;
-    if (!mbar_wait(bar_base + 8 * (kBarEmpty + stage), par ^ 1u, abort, a.status)) continue;
-    dequant_kstep<Q>(cur, r, a_base + stage * kAStage, bc);
+    const uint32_t ps = it % NPS, pp = (it / NPS) & 1u;
+    const uint32_t st = it % NST, sp = (it / NST) & 1u;
+    if (!mbar_wait(bar_base + 8 * (kBarPlFull + ps), pp, abort, a.status)) break;
+    const uint32_t pbase = kOffPlanes + ps * kPlaneStage + d.word * 4;
+    uint32_t wd[Q];
+#pragma unroll
+    for (int p = 0; p < Q; ++p) wd[p] = *reinterpret_cast<const uint32_t*>(g_psmem + pbase + p * 512);
+    mbar_arrive(bar_base + 8 * (kBarPlEmpty + ps));
+    uint32_t ib[4];
+    planes_to_index_half<Q>(wd, sel, ib, bc);
+    if (!mbar_wait(bar_base + 8 * (kBarEmpty + st), sp ^ 1u, abort, a.status)) break;
+    const uint32_t row_base = sbase + kOffA + st * kAStage + d.r * 64;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {   // 16-byte chunk 2*half + cc = 8 columns
+      uint32_t packed[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t word = ib[2 * cc + h];
+        uint32_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t off = __byte_perm(word, d.slot, 0x6504 | (j << 4));
+          v[j] = *reinterpret_cast<const uint16_t*>(g_psmem + off);
+        }
+        packed[2 * h] = __byte_perm(v[0], v[1], 0x5410);
+        packed[2 * h + 1] = __byte_perm(v[2], v[3], 0x5410);
+      }
+      const uint32_t c = 2 * half + cc;
+      const uint32_t dst = row_base + ((c ^ sw) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[0]),
+                   "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
+                   : "memory");
+    }
     fence_proxy_async();
-    mbar_arrive(bar_base + 8 * (kBarFullA + stage));
+    mbar_arrive(bar_base + 8 * (kBarFullA + st));
   }
+}
+
+template <int Q>
+__device__ __forceinline__ void dequant_tile(const GemmArgs& a, Mode mode, const pw_block_entry& ent,
+                                             const DqRow& d, int ksteps, uint32_t it_base, int set,
+                                             int half, uint32_t sbase, uint32_t bar_base,
+                                             volatile int* abort, const BitConsts& bc) {
+  load_lut<Q>(ent.lut, d.grow, d.slot, 2 * set + half);
+  named_sync_dq();
+  dequant_ksteps<Q>(a, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc);
 }
 
 // ---------------------------------------------------------------- epilogue
 
-__device__ void epilogue(const GemmArgs& a, Mode mode, const Tile& tile, int pos0, int ntok,
-                         bool usable, uint32_t tmem_base, int quarter, int lane, uint32_t bar_base,
-                         uint32_t acc_par, volatile int* abort) {
-  const int r = quarter * 32 + lane;
-  if (usable) {
-    if (*abort || !mbar_wait(bar_base + 8 * kBarAccFull, acc_par, abort, a.status)) return;
-    tc_fence_after();
+// gate_up: thread (quarter q, lane L) holds TMEM lane 32q + L.  Lanes L and
+// L ^ 8 hold the gate and up rows of h column 16q + 8(L / 16) + L % 8; the
+// gate lane finishes the even tokens, the up lane the odd ones.
+__device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, int ntok,
+                                uint32_t tmem_base, int quarter, int lane, int tid_e,
+                                uint32_t sbase, uint32_t& chunk_seq) {
+  const int up = (lane >> 3) & 1;
+  const int hc = 16 * quarter + 8 * (lane >> 4) + (lane & 7);
+  for (int c = 0; c < BN / 32; ++c) {
+    if (c * 32 >= ntok) break;
+    float v[32];
+    tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
+    const uint32_t buf = sbase + kOffStage + (chunk_seq & 1u) * kStageBuf;
+    ++chunk_seq;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float send = up ? v[2 * j] : v[2 * j + 1];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
+      const float g = up ? recv : v[2 * j];
+      const float u = up ? v[2 * j + 1] : recv;
+      const float h = __fdividef(g, 1.f + __expf(-g)) * u;
+      const int tok = 2 * j + up;
+      st_shared_u16(buf + (tok * 64 + hc) * 2, __half_as_ushort(__float2half_rn(h)));
+    }
+    named_sync_epi();
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int piece = tid_e + 128 * k2, tok = piece >> 3, part = piece & 7;
+      const int n = c * 32 + tok;
+      if (n < ntok) {
+        uint4 val;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                     : "r"(buf + tok * 128 + part * 16));
+        *reinterpret_cast<uint4*>(a.h_ws + static_cast<long long>(pos0 + n) * a.I + tile.m * 64 +
+                                  part * 8) = val;
+      }
+    }
   }
+}
+
+// down: thread (quarter q, lane L) holds row 128 m + 32 q + L of y; a warp's
+// stores for one token are one 128-byte line.  Tiles of an expert that cannot
+// be computed write zeros.
+__device__ void epilogue_down(const GemmArgs& a, const Tile& tile, int pos0, int ntok, bool usable,
+                              uint32_t tmem_base, int quarter, int lane) {
+  const int row = tile.m * BM + quarter * 32 + lane;
   for (int c = 0; c < BN / 32; ++c) {
     if (c * 32 >= ntok) break;
     float v[32];
@@ -388,34 +530,14 @@ __device__ void epilogue(const GemmArgs& a, Mode mode, const Tile& tile, int pos
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = 0.f;
     }
-    if (mode == kGateUp) {
-      if (!usable) continue;  // h of a skipped expert is never read
-      const int col = tile.m * 64 + (r >> 1);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
-        const int n = c * 32 + j;
-        if ((lane & 1) == 0 && n < ntok) {
-          const float g = v[j], u = other;
-          const float h = g / (1.f + expf(-g)) * u;
-          a.h_ws[static_cast<long long>(pos0 + n) * a.I + col] = __float2half_rn(h);
-        }
-      }
-    } else {
-      const int row = tile.m * BM + r;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int n = c * 32 + j;
-        if (n < ntok) {
-          const int pair = a.perm[pos0 + n];
-          a.y_ws[static_cast<long long>(pair) * a.H + row] = v[j];
-        }
+    for (int j = 0; j < 32; ++j) {
+      const int n = c * 32 + j;
+      if (n < ntok) {
+        const int pair = a.perm[pos0 + n];
+        a.y_ws[static_cast<long long>(pair) * a.H + row] = v[j];
       }
     }
-  }
-  if (usable) {
-    tc_fence_before();
-    mbar_arrive(bar_base + 8 * kBarAccEmpty);
   }
 }
 
@@ -430,6 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_base = sbase + kOffBar;
   uint32_t* misc = reinterpret_cast<uint32_t*>(g_psmem + kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(misc + 1);
+  volatile int* ring = reinterpret_cast<volatile int*>(misc + 2);
+  volatile int* dq_slot = reinterpret_cast<volatile int*>(misc + 6);
+  volatile int* epi_slot = reinterpret_cast<volatile int*>(misc + 8);
   int* prefix = reinterpret_cast<int*>(g_psmem + kOffPrefix);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = m_tiles(mode, a);
@@ -449,9 +574,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     prefix[a.E] = run;
     for (int i = 0; i < NST; ++i) {
-      mbar_init(bar_base + 8 * (kBarFullA + i), kDqThreads / 2);
+      mbar_init(bar_base + 8 * (kBarFullA + i), kSetThreads);
       mbar_init(bar_base + 8 * (kBarFullB + i), 1);
       mbar_init(bar_base + 8 * (kBarEmpty + i), 1);
+    }
+    for (int i = 0; i < NPS; ++i) {
+      mbar_init(bar_base + 8 * (kBarPlFull + i), 1);
+      mbar_init(bar_base + 8 * (kBarPlEmpty + i), kSetThreads);
+    }
+    for (int i = 0; i < kTileRing; ++i) {
+      mbar_init(bar_base + 8 * (kBarTileFull + i), 1);
+      mbar_init(bar_base + 8 * (kBarTileEmpty + i), kTileConsumers);
     }
     mbar_init(bar_base + 8 * kBarAccFull, 1);
     mbar_init(bar_base + 8 * kBarAccEmpty, 128);
@@ -471,75 +604,152 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = misc[0];
   const int total = prefix[a.E];
 
-  if (warp < 8) {
-    // ---- dequant producers: set 0 = warps 0-3 (even k-steps), set 1 = warps 4-7
-    const int set = warp >> 2, r = tid & 127;
-    uint32_t it_base = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+  if (warp < kDqWarps) {
+    // ---- dequant: set 0 = warps 0-7 (even k-steps), set 1 = warps 8-15
+    const int set = warp >> 3, half = (warp >> 2) & 1, w = warp & 3;
+    uint32_t it_base = 0, seq = 0, iter = 0;
+    for (;; ++iter) {
+      if (tid == 0) dq_slot[iter & 1] = ring_take(bar_base, ring, seq, abort, a.status);
+      named_sync_dq();   // the previous tile's lookups are done; the tile id is visible
+      const int t = dq_slot[iter & 1];
+      if (t >= total) break;
       const Tile tile = tile_at(t, prefix, a.E, a.offsets);
-      const bool usable = tile_usable(mode, a, tile.e);
-      if (!usable) continue;
+      if (!tile_usable(mode, a, tile.e)) continue;
       const pw_block_entry ent = a.table[2 * tile.e + (mode == kGateUp ? 0 : 1)];
+      const DqRow d = dq_row(mode, a, tile.m, w, lane);
       switch (ent.q) {
-        case 3: dequant_tile<3>(a, mode, ent, tile.m, ksteps, it_base, set, r, bar_base, abort, bc); break;
-        case 4: dequant_tile<4>(a, mode, ent, tile.m, ksteps, it_base, set, r, bar_base, abort, bc); break;
-        case 5: dequant_tile<5>(a, mode, ent, tile.m, ksteps, it_base, set, r, bar_base, abort, bc); break;
-        case 6: dequant_tile<6>(a, mode, ent, tile.m, ksteps, it_base, set, r, bar_base, abort, bc); break;
-        default: dequant_tile<8>(a, mode, ent, tile.m, ksteps, it_base, set, r, bar_base, abort, bc); break;
+        case 3: dequant_tile<3>(a, mode, ent, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc); break;
+        case 4: dequant_tile<4>(a, mode, ent, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc); break;
+        case 5: dequant_tile<5>(a, mode, ent, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc); break;
+        case 6: dequant_tile<6>(a, mode, ent, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc); break;
+        default: dequant_tile<8>(a, mode, ent, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc); break;
       }
       it_base += ksteps;
     }
-  } else if (warp < kTmaWarp) {
+  } else if (warp < kSchedWarp) {
     // ---- epilogue
-    const int quarter = warp - kEpiWarp0;
-    uint32_t acc_it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    const int quarter = warp & 3, tid_e = tid - kEpiWarp0 * 32;
+    volatile int* acc_ok = reinterpret_cast<volatile int*>(misc + 10);
+    uint32_t acc_it = 0, seq = 0, iter = 0, chunk_seq = 0;
+    for (;; ++iter) {
+      if (tid_e == 0) epi_slot[iter & 1] = ring_take(bar_base, ring, seq, abort, a.status);
+      named_sync_epi();
+      const int t = epi_slot[iter & 1];
+      if (t >= total) break;
       const Tile tile = tile_at(t, prefix, a.E, a.offsets);
       const int pos0 = a.offsets[tile.e] + tile.n * BN;
       const int ntok = min(BN, a.offsets[tile.e + 1] - pos0);
       const bool usable = tile_usable(mode, a, tile.e);
-      if (!usable && quarter == 0 && lane == 0) report_unusable(mode, a, tile.e);
-      epilogue(a, mode, tile, pos0, ntok, usable, tmem_base, quarter, lane, bar_base, acc_it & 1u,
-               abort);
-      if (usable) ++acc_it;
+      if (!usable) {
+        if (tid_e == 0) report_unusable(mode, a, tile.e);
+        if (mode == kDown) epilogue_down(a, tile, pos0, ntok, false, tmem_base, quarter, lane);
+        continue;
+      }
+      if (tid_e == 0)
+        *acc_ok = mbar_wait(bar_base + 8 * kBarAccFull, acc_it & 1u, abort, a.status) ? 1 : 0;
+      ++acc_it;
+      named_sync_epi();
+      if (!*acc_ok) break;
+      tc_fence_after();
+      if (mode == kGateUp)
+        epilogue_gateup(a, tile, pos0, ntok, tmem_base, quarter, lane, tid_e, sbase, chunk_seq);
+      else
+        epilogue_down(a, tile, pos0, ntok, true, tmem_base, quarter, lane);
+      tc_fence_before();
+      mbar_arrive(bar_base + 8 * kBarAccEmpty);
     }
-  } else if (warp == kTmaWarp) {
-    // ---- TMA producer for the token operand
+  } else if (warp == kSchedWarp) {
+    // ---- scheduler + TMA producer for the token operand
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
-      uint32_t it = 0;
-      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+      uint32_t it = 0, seq = 0;
+      for (;;) {
+        const uint32_t slot = seq % kTileRing, par = (seq / kTileRing) & 1u;
+        ++seq;
+        if (!mbar_wait(bar_base + 8 * (kBarTileEmpty + slot), par ^ 1u, abort, a.status)) break;
+        int t = atomicAdd(a.tile_counter, 1);
+        if (t >= total) t = INT_MAX;
+        ring[slot] = t;
+        mbar_arrive(bar_base + 8 * (kBarTileFull + slot));
+        if (t == INT_MAX) break;
         const Tile tile = tile_at(t, prefix, a.E, a.offsets);
         if (!tile_usable(mode, a, tile.e)) continue;
         const int pos0 = a.offsets[tile.e] + tile.n * BN;
         const int ntok = min(BN, a.offsets[tile.e + 1] - pos0);
         const int halves = ntok > BNH ? 2 : 1;
+        bool ok = true;
         for (int s = 0; s < ksteps; ++s, ++it) {
-          const int stage = it % NST;
-          const uint32_t par = (it / NST) & 1u;
-          if (!mbar_wait(bar_base + 8 * (kBarEmpty + stage), par ^ 1u, abort, a.status)) break;
+          const uint32_t stage = it % NST, spar = (it / NST) & 1u;
+          if (!mbar_wait(bar_base + 8 * (kBarEmpty + stage), spar ^ 1u, abort, a.status)) {
+            ok = false;
+            break;
+          }
           const uint32_t full = bar_base + 8 * (kBarFullB + stage);
           mbar_arrive_tx(full, halves * kBHalf);
           for (int h = 0; h < halves; ++h)
             tma_load_2d(sbase + kOffB + stage * kBStage + h * kBHalf, &tmap_b, s * BK,
                         pos0 + h * BNH, full);
         }
+        if (!ok) break;
       }
-      if (*abort) {
-        // let the copies this thread issued land before the CTA unwinds
-        for (uint32_t j = (it > NST ? it - NST : 0); j < it; ++j) {
-          const uint32_t bar = bar_base + 8 * (kBarFullB + j % NST);
-          for (uint32_t i = 0; i < kSpinLimit && !mbar_try(bar, (j / NST) & 1u); ++i) {
+      if (*abort) drain_copies(bar_base, kBarFullB, NST, it, NST);
+    }
+  } else if (warp == kPlaneWarp) {
+    // ---- plane producer: lane 0 takes tiles and arms the stage barriers;
+    // the copies of a k-step are issued by the lanes in parallel (one per
+    // lane), which keeps the copy engine fed.
+    {
+      uint32_t pit = 0, seq = 0;
+      const long long N = (mode == kGateUp) ? 2LL * a.I : a.H;
+      const long long plane_stride = N * ksteps;
+      for (;;) {
+        int t0 = 0;
+        if (lane == 0) t0 = ring_take(bar_base, ring, seq, abort, a.status);
+        const int t = __shfl_sync(0xffffffffu, t0, 0);
+        if (t >= total) break;
+        const Tile tile = tile_at(t, prefix, a.E, a.offsets);
+        if (!tile_usable(mode, a, tile.e)) continue;
+        const pw_block_entry ent = a.table[2 * tile.e + (mode == kGateUp ? 0 : 1)];
+        const int q = ent.q;
+        const uint32_t* base =
+            ent.planes + ((mode == kGateUp) ? static_cast<long long>(tile.m) * 64
+                                            : static_cast<long long>(tile.m) * BM);
+        bool ok = true;
+        for (int s = 0; s < ksteps; ++s, ++pit) {
+          const uint32_t ps = pit % NPS, pp = (pit / NPS) & 1u;
+          int ok0 = 1;
+          if (lane == 0) ok0 = mbar_wait(bar_base + 8 * (kBarPlEmpty + ps), pp ^ 1u, abort, a.status);
+          if (!__shfl_sync(0xffffffffu, ok0, 0)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = bar_base + 8 * (kBarPlFull + ps);
+          const uint32_t dst = sbase + kOffPlanes + ps * kPlaneStage;
+          if (lane == 0) mbar_arrive_tx(full, static_cast<uint32_t>(q) * 512u);
+          __syncwarp();
+          const uint32_t* col = base + static_cast<long long>(s) * N;
+          if (mode == kGateUp) {
+            if (lane < 2 * q) {   // lane 2p + seg: plane p, gate (0) or up (1) run
+              const int p = lane >> 1, seg = lane & 1;
+              bulk_copy(dst + p * 512 + seg * 256, col + p * plane_stride + (seg ? a.I : 0), 256,
+                        full);
+            }
+          } else if (lane < q) {
+            bulk_copy(dst + lane * 512, col + lane * plane_stride, 512, full);
           }
         }
+        if (!ok) break;
       }
+      if (*abort && lane == 0) drain_copies(bar_base, kBarPlFull, NPS, pit, NPS);
     }
   } else {
     // ---- MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, acc_it = 0;
+      uint32_t it = 0, acc_it = 0, seq = 0;
       bool issued = false;
-      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+      for (;;) {
+        const int t = ring_take(bar_base, ring, seq, abort, a.status);
+        if (t >= total) break;
         const Tile tile = tile_at(t, prefix, a.E, a.offsets);
         if (!tile_usable(mode, a, tile.e)) continue;
         const int pos0 = a.offsets[tile.e] + tile.n * BN;
@@ -549,11 +759,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t id0 = make_idesc(n0), id1 = make_idesc(n1 > 0 ? n1 : 16);
         if (!mbar_wait(bar_base + 8 * kBarAccEmpty, (acc_it & 1u) ^ 1u, abort, a.status)) break;
         tc_fence_after();
+        bool ok = true;
         for (int s = 0; s < ksteps; ++s, ++it) {
-          const int stage = it % NST;
-          const uint32_t par = (it / NST) & 1u;
-          if (!mbar_wait(bar_base + 8 * (kBarFullA + stage), par, abort, a.status)) break;
-          if (!mbar_wait(bar_base + 8 * (kBarFullB + stage), par, abort, a.status)) break;
+          const uint32_t stage = it % NST, par = (it / NST) & 1u;
+          if (!mbar_wait(bar_base + 8 * (kBarFullA + stage), par, abort, a.status) ||
+              !mbar_wait(bar_base + 8 * (kBarFullB + stage), par, abort, a.status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t a_addr = sbase + kOffA + stage * kAStage;
           const uint32_t b_addr = sbase + kOffB + stage * kBStage;
@@ -568,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued = true;
           mma_commit(bar_base + 8 * (kBarEmpty + stage));
         }
-        if (*abort) break;
+        if (!ok) break;
         mma_commit(bar_base + 8 * kBarAccFull);
         ++acc_it;
       }
@@ -593,12 +806,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------- gather / combine
 
 // xg[pos][c] = fp16(hidden[perm[pos] / k][c]); positions past the routed
-// pairs are zero.  8 columns per thread.
+// pairs are zero.  8 columns per thread.  Also resets the GEMMs' tile counters.
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ hidden,
                                                      const int32_t* __restrict__ perm,
                                                      const int32_t* __restrict__ offsets, int E,
                                                      int k, int H, int n_pairs,
-                                                     __half* __restrict__ xg) {
+                                                     __half* __restrict__ xg,
+                                                     int32_t* __restrict__ counters) {
+  if (blockIdx.x == 0 && threadIdx.x < 2) counters[threadIdx.x] = 0;
   const long long per_row = H / 8;
   const long long total = static_cast<long long>(n_pairs) * per_row;
   const int valid = offsets[E];
@@ -646,6 +861,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
+  int32_t* counters;   // [2] tile counters of the two GEMM launches
   int32_t* offsets;
   int32_t* perm;
   __half* xg;
@@ -657,6 +873,8 @@ WsLayout carve_ws(void* ws, const pw_moe_shape& s) {
   const size_t P = static_cast<size_t>(s.T) * s.k;
   char* p = static_cast<char*>(ws);
   WsLayout w;
+  w.counters = reinterpret_cast<int32_t*>(p);
+  p += 256;
   w.offsets = reinterpret_cast<int32_t*>(p);
   p += round256(sizeof(int32_t) * (s.E + 1));
   w.perm = reinterpret_cast<int32_t*>(p);
@@ -712,7 +930,7 @@ int num_sms() {
 
 size_t prefill_workspace_bytes(const pw_moe_shape& s) {
   const size_t P = static_cast<size_t>(s.T) * s.k;
-  return round256(sizeof(int32_t) * (s.E + 1)) + round256(sizeof(int32_t) * P) +
+  return 256 + round256(sizeof(int32_t) * (s.E + 1)) + round256(sizeof(int32_t) * P) +
          round256(2 * P * s.H) + round256(2 * P * s.I) + round256(4 * P * s.H);
 }
 
@@ -744,7 +962,7 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   const long long gwork = static_cast<long long>(n_pairs) * (la.H / 8);
   const int gblocks = static_cast<int>(std::min<long long>((gwork + 255) / 256, 152LL * 32));
   gather_kernel<<<gblocks, 256, 0, stream>>>(la.hidden, w.perm, w.offsets, la.E, la.k, la.H,
-                                             n_pairs, w.xg);
+                                             n_pairs, w.xg, w.counters);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   CUtensorMap map_x, map_h;
@@ -764,8 +982,10 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   g.status = la.status;
   const int grid = num_sms();
   const BitConsts bc = make_bit_consts();
+  g.tile_counter = w.counters;
   dq_gemm_kernel<kGateUp><<<grid, kThreads, kSmemBytes, stream>>>(g, map_x, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  g.tile_counter = w.counters + 1;
   dq_gemm_kernel<kDown><<<grid, kThreads, kSmemBytes, stream>>>(g, map_h, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long cwork = static_cast<long long>(la.T) * la.H;
