@@ -8,8 +8,14 @@
 //
 //   prep:    CTA 0 groups the (token, expert) pairs by expert (stable), lists
 //            the routed experts largest-bitwidth first (so the costliest
-//            tiles are scheduled first), and resets the tile counters; the
-//            other CTAs widen the hidden states to fp32 and zero `out`.
+//            tiles are scheduled first) with each one's page-table entry,
+//            and resets the tile counters; the other CTAs widen the hidden
+//            states to fp32 and zero `out`.
+//   [heavy]  experts holding at least kHeavyMinTokens pairs are left out of
+//            those lists: the tcgen05 GEMM kernels of the prefill path run
+//            them (gather, gate_up, down -> y) between prep and gate_up, so
+//            their planes are read and dequantised once instead of once per
+//            group of 4 tokens.
 //   gate_up: persistent CTAs take tiles (routed expert, 32 gate/up row pairs)
 //            from an atomic counter: read the top q planes of gate rows i and
 //            up rows I+i, rebuild the q-bit codes, look them up in each row's
@@ -93,6 +99,21 @@ __device__ __forceinline__ SmemPtrs carve(unsigned char* base) {
   return s;
 }
 
+// One routed expert's share of a kernel, written by the prep launch so that a
+// tile needs one dependent load: the expert, its grouped pair positions and
+// the page-table entry of the kernel's block (copied at prep time; the table
+// changes only between calls).
+struct SlotInfo {
+  int32_t e;        // expert id
+  int32_t off;      // first grouped pair position of e
+  int32_t ne;       // pairs routed to e
+  int32_t q;        // committed bitwidth of the block
+  int32_t err;      // 0 if the tiles can run, else the status to latch
+  int32_t pad;
+  const uint32_t* planes;
+  const uint16_t* lut;
+};
+
 // Workspace of one decode call.
 struct DecodeWs {
   float* x32;      // [T][H]   hidden states widened to fp32
@@ -100,10 +121,11 @@ struct DecodeWs {
   float* y;        // [P][H]   expert output, by pair id
   int* offsets;    // [E+1]    expert e owns grouped positions offsets[e] .. offsets[e+1]
   int* perm;       // [P]      grouped position -> pair id
-  int* routed_gu;  // [E]      routed experts, gate_up bitwidth descending
-  int* routed_dn;  // [E]      routed experts, down bitwidth descending
+  SlotInfo* routed_gu;  // [E] routed experts, gate_up bitwidth descending
+  SlotInfo* routed_dn;  // [E] routed experts, down bitwidth descending
   int* ctl;        // [0] routed expert count, [1] gate_up tile counter, [2] down tile counter
   int* arrive;     // [H/32]   per 64-row range: down tiles finished
+  int heavy_min;   // experts with at least this many pairs are left to the GEMM kernels (0: none)
 };
 
 // Rows streamed by one pass: lane L of row slot g owns row
@@ -164,25 +186,40 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // LUT rows of one pass into shared memory as fp32 (layouts above).  Each
-// thread moves 8 fp16 entries (16 bytes); a warp's stores hit 32 banks.
+// thread moves up to four 16-byte pieces (8 fp16 entries each); all of its
+// loads are issued before the first store, so a pass waits for one memory
+// round trip.  A warp's stores hit 32 banks.
 template <int Q, int R, bool COMPACT>
 __device__ __forceinline__ void load_luts(const uint16_t* lut, const PassRows<R>& pr,
                                           const SmemPtrs& s) {
   constexpr int kEnt = 1 << Q;
   constexpr int kVecPerRow = kEnt / 8;
+  constexpr int kPerSlot = 32 * kVecPerRow;
+  constexpr int kTotal = R * kPerSlot;
+  constexpr int kPer = (kTotal + kThreads - 1) / kThreads;
+  uint4 raw[kPer];
 #pragma unroll
-  for (int g = 0; g < R; ++g) {
-    for (int i = threadIdx.x; i < 32 * kVecPerRow; i += kThreads) {
-      const int L = i & 31, vec = i >> 5;
+  for (int j = 0; j < kPer; ++j) {
+    const int i = threadIdx.x + j * kThreads;
+    if (i < kTotal) {
+      const int g = i / kPerSlot, rem = i % kPerSlot;
+      const int L = rem & 31, vec = rem >> 5;
       const int row = seg_base<R>(pr, g, L >> 4) + (L & 15);
-      const uint4 raw =
-          __ldg(reinterpret_cast<const uint4*>(lut + static_cast<long long>(row) * kEnt + vec * 8));
-      const __half* h = reinterpret_cast<const __half*>(&raw);
+      raw[j] = __ldg(reinterpret_cast<const uint4*>(lut + static_cast<long long>(row) * kEnt + vec * 8));
+    }
+  }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int v = vec * 8 + j;
+  for (int j = 0; j < kPer; ++j) {
+    const int i = threadIdx.x + j * kThreads;
+    if (i < kTotal) {
+      const int g = i / kPerSlot, rem = i % kPerSlot;
+      const int L = rem & 31, vec = rem >> 5;
+      const __half* h = reinterpret_cast<const __half*>(&raw[j]);
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int v = vec * 8 + jj;
         const int off = COMPACT ? v * 128 + L * 4 : v * 256 + g * 128 + L * 4;
-        *reinterpret_cast<float*>(g_dsmem + off) = __half2float(h[j]);
+        *reinterpret_cast<float*>(g_dsmem + off) = __half2float(h[jj]);
       }
     }
   }
@@ -282,13 +319,32 @@ __device__ __forceinline__ void compute_column(uint32_t stage, int lane, const B
   }
 }
 
+// Start the copies of the warp's first kStages - 1 word columns (one commit
+// group each), so that their latency can overlap other set-up work.
+template <int Q, int R, int NT>
+__device__ __forceinline__ void ring_prime(const uint32_t* planes, long long plane_stride,
+                                           long long N, const PassRows<R>& pr, int kw_lo,
+                                           int kw_hi, const float* const (&xs)[NT], int nt) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = kw_hi - kw_lo;
+  if (n <= 0) return;
+  const uint32_t ring_s = smem_u32(g_dsmem) + kOffRing + warp * (kStages * kStageBytes);
+  const CopyPlan<Q, R, NT> plan = make_copy_plan<Q, R, NT>(plane_stride, pr, xs, nt, lane);
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) {
+    if (i < n) issue_column<Q, R, NT>(ring_s + i * kStageBytes, planes, N, plan, kw_lo + i, lane);
+    cp_async_commit();
+  }
+}
+
 // Partial dot products of this lane's rows over the warp's word columns
-// [kw_lo, kw_hi), streamed through the warp's kStages-deep cp.async ring.
+// [kw_lo, kw_hi), streamed through the warp's kStages-deep cp.async ring
+// (whose first columns were already started when `primed`).
 template <int Q, int R, int NT, bool COMPACT>
 __device__ __forceinline__ void rows_dot(const uint32_t* planes, long long plane_stride, long long N,
                                          const PassRows<R>& pr, int kw_lo, int kw_hi,
                                          const float* const (&xs)[NT], int nt, const SmemPtrs& s,
-                                         const BitConsts& bc, float2 (&acc)[R][NT]) {
+                                         const BitConsts& bc, float2 (&acc)[R][NT], bool primed) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int g = 0; g < R; ++g)
@@ -299,11 +355,7 @@ __device__ __forceinline__ void rows_dot(const uint32_t* planes, long long plane
   const uint32_t ring = kOffRing + warp * (kStages * kStageBytes);   // offset in g_dsmem
   const uint32_t ring_s = smem_u32(g_dsmem) + ring;
   const CopyPlan<Q, R, NT> plan = make_copy_plan<Q, R, NT>(plane_stride, pr, xs, nt, lane);
-#pragma unroll
-  for (int i = 0; i < kStages - 1; ++i) {
-    if (i < n) issue_column<Q, R, NT>(ring_s + i * kStageBytes, planes, N, plan, kw_lo + i, lane);
-    cp_async_commit();
-  }
+  if (!primed) ring_prime<Q, R, NT>(planes, plane_stride, N, pr, kw_lo, kw_hi, xs, nt);
   for (int i = 0; i < n; ++i) {
     const int pf = i + kStages - 1;
     if (pf < n)
@@ -324,9 +376,11 @@ __device__ __forceinline__ void warp_range(int KW, int& lo, int& hi) {
 }
 
 
-// Broadcast the next tile id from a global counter to the whole CTA.
-__device__ __forceinline__ int next_tile(int* counter, int* slot) {
-  if (threadIdx.x == 0) *slot = atomicAdd(counter, 1);
+// Tile ids: a CTA's first tile is its block index; later ones come from a
+// global counter (offset by the grid size) and are broadcast to the CTA.
+__device__ __forceinline__ int next_tile(int* counter, int* slot, bool first) {
+  if (first) return blockIdx.x;
+  if (threadIdx.x == 0) *slot = gridDim.x + atomicAdd(counter, 1);
   __syncthreads();
   const int t = *slot;
   __syncthreads();
@@ -338,21 +392,40 @@ __device__ __forceinline__ int next_tile(int* counter, int* slot) {
 // One token group of one pass.  Paired passes (R = 2): slot 0 = gate rows
 // hcol0 + L, slot 1 = up rows I + hcol0 + L.  Compact passes (R = 1): lanes
 // 0-15 gate rows hcol0 + L, lanes 16-31 the matching up rows.
+template <int NT>
+__device__ __forceinline__ void gateup_xs(const LayerArgs& a, const DecodeWs& w,
+                                          const ExpertWork& ex, int g0, int nt,
+                                          const float* (&xs)[NT]) {
+#pragma unroll
+  for (int tk = 0; tk < NT; ++tk)
+    xs[tk] = w.x32 + static_cast<long long>(w.perm[ex.off + g0 + min(tk, nt - 1)] / a.k) * a.H;
+}
+
+template <int Q, int R, int NT>
+__device__ void gateup_prime(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
+                             const SlotInfo& ent, const PassRows<R>& pr, int g0, int nt) {
+  const int KW = a.H / 32;
+  const long long N = 2LL * a.I;
+  int lo, hi;
+  warp_range(KW, lo, hi);
+  const float* xs[NT];
+  gateup_xs<NT>(a, w, ex, g0, nt, xs);
+  ring_prime<Q, R, NT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt);
+}
+
 template <int Q, int R, bool COMPACT, int NT>
 __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
-                             const pw_block_entry& ent, const PassRows<R>& pr, int hcol0, int g0,
-                             int nt, const SmemPtrs& s, const BitConsts& bc) {
+                             const SlotInfo& ent, const PassRows<R>& pr, int hcol0, int g0,
+                             int nt, const SmemPtrs& s, const BitConsts& bc, bool primed) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int KW = a.H / 32;
   const long long N = 2LL * a.I;
   int lo, hi;
   warp_range(KW, lo, hi);
   const float* xs[NT];
-#pragma unroll
-  for (int tk = 0; tk < NT; ++tk)
-    xs[tk] = w.x32 + static_cast<long long>(w.perm[ex.off + g0 + min(tk, nt - 1)] / a.k) * a.H;
+  gateup_xs<NT>(a, w, ex, g0, nt, xs);
   float2 acc[R][NT];
-  rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc);
+  rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc, primed);
 #pragma unroll
   for (int tk = 0; tk < NT; ++tk)
 #pragma unroll
@@ -379,22 +452,28 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
 
 template <int Q, int R, bool COMPACT>
 __device__ void gateup_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
-                            const pw_block_entry& ent, const PassRows<R>& pr, int hcol0,
+                            const SlotInfo& ent, const PassRows<R>& pr, int hcol0,
                             const SmemPtrs& s, const BitConsts& bc) {
-  __syncthreads();  // the previous pass is done with the LUT region
+  __syncthreads();  // the previous pass is done with the LUT region and the rings
+  // the first token group's first columns start loading before the LUT does
+  const int nt0 = min(kTG, ex.ne);
+  if (nt0 == 1) gateup_prime<Q, R, 1>(a, w, ex, ent, pr, 0, nt0);
+  else if (nt0 == 2) gateup_prime<Q, R, 2>(a, w, ex, ent, pr, 0, nt0);
+  else gateup_prime<Q, R, 4>(a, w, ex, ent, pr, 0, nt0);
   load_luts<Q, R, COMPACT>(ent.lut, pr, s);
   __syncthreads();
   for (int g0 = 0; g0 < ex.ne; g0 += kTG) {
     const int nt = min(kTG, ex.ne - g0);
-    if (nt == 1) gateup_group<Q, R, COMPACT, 1>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc);
-    else if (nt == 2) gateup_group<Q, R, COMPACT, 2>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc);
-    else gateup_group<Q, R, COMPACT, 4>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc);
+    const bool primed = (g0 == 0);
+    if (nt == 1) gateup_group<Q, R, COMPACT, 1>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed);
+    else if (nt == 2) gateup_group<Q, R, COMPACT, 2>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed);
+    else gateup_group<Q, R, COMPACT, 4>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed);
   }
 }
 
 template <int Q>
 __device__ void gateup_tile(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
-                            const pw_block_entry& ent, int i0, const SmemPtrs& s,
+                            const SlotInfo& ent, int i0, const SmemPtrs& s,
                             const BitConsts& bc) {
   if (Q == 8) {
 #pragma unroll 1
@@ -423,48 +502,62 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerA
   allow_dependent_launch();    // the down kernel may start loading as CTAs retire
   const int tpe = a.I / kPairsPerTile;
   const int total = w.ctl[0] * tpe;
-  for (;;) {
-    const int t = next_tile(&w.ctl[1], &s.misc[0]);
+  for (bool first = true;; first = false) {
+    const int t = next_tile(&w.ctl[1], &s.misc[0], first);
     if (t >= total) break;
     const int slot = t / tpe, x = t - slot * tpe;
-    ExpertWork ex;
-    ex.e = w.routed_gu[slot];
-    ex.off = w.offsets[ex.e];
-    ex.ne = w.offsets[ex.e + 1] - ex.off;
-    const pw_block_entry ent = a.table[2 * ex.e];
-    if (ent.state != PW_PAGE_GPU) {
-      if (x == 0 && threadIdx.x == 0) latch_status(a.status, PW_ERR_PAGE_NOT_RESIDENT);
+    const SlotInfo si = w.routed_gu[slot];
+    if (si.err) {
+      if (x == 0 && threadIdx.x == 0) latch_status(a.status, si.err);
       continue;
     }
-    switch (ent.q) {
-      case 3: gateup_tile<3>(a, w, ex, ent, x * kPairsPerTile, s, bc); break;
-      case 4: gateup_tile<4>(a, w, ex, ent, x * kPairsPerTile, s, bc); break;
-      case 5: gateup_tile<5>(a, w, ex, ent, x * kPairsPerTile, s, bc); break;
-      case 6: gateup_tile<6>(a, w, ex, ent, x * kPairsPerTile, s, bc); break;
-      case 8: gateup_tile<8>(a, w, ex, ent, x * kPairsPerTile, s, bc); break;
-      default:
-        if (x == 0 && threadIdx.x == 0) latch_status(a.status, PW_ERR_UNSUPPORTED_Q);
+    const ExpertWork ex{si.e, si.off, si.ne};
+    switch (si.q) {
+      case 3: gateup_tile<3>(a, w, ex, si, x * kPairsPerTile, s, bc); break;
+      case 4: gateup_tile<4>(a, w, ex, si, x * kPairsPerTile, s, bc); break;
+      case 5: gateup_tile<5>(a, w, ex, si, x * kPairsPerTile, s, bc); break;
+      case 6: gateup_tile<6>(a, w, ex, si, x * kPairsPerTile, s, bc); break;
+      default: gateup_tile<8>(a, w, ex, si, x * kPairsPerTile, s, bc); break;
     }
   }
 }
 
 // ---------------------------------------------------------------- down
 
+template <int NT>
+__device__ __forceinline__ void down_xs(const LayerArgs& a, const DecodeWs& w,
+                                        const ExpertWork& ex, int g0, int nt,
+                                        const float* (&xs)[NT]) {
+#pragma unroll
+  for (int tk = 0; tk < NT; ++tk)
+    xs[tk] = w.h + static_cast<long long>(ex.off + g0 + min(tk, nt - 1)) * a.I;
+}
+
+template <int Q, int R, int NT>
+__device__ void down_prime(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
+                           const SlotInfo& ent, const PassRows<R>& pr, int g0, int nt) {
+  const int KW = a.I / 32;
+  const long long N = a.H;
+  int lo, hi;
+  warp_range(KW, lo, hi);
+  const float* xs[NT];
+  down_xs<NT>(a, w, ex, g0, nt, xs);
+  ring_prime<Q, R, NT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt);
+}
+
 template <int Q, int R, bool COMPACT, int NT>
 __device__ void down_group(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
-                           const pw_block_entry& ent, const PassRows<R>& pr, int g0, int nt,
-                           const SmemPtrs& s, const BitConsts& bc) {
+                           const SlotInfo& ent, const PassRows<R>& pr, int g0, int nt,
+                           const SmemPtrs& s, const BitConsts& bc, bool primed) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int KW = a.I / 32;
   const long long N = a.H;
   int lo, hi;
   warp_range(KW, lo, hi);
   const float* xs[NT];
-#pragma unroll
-  for (int tk = 0; tk < NT; ++tk)
-    xs[tk] = w.h + static_cast<long long>(ex.off + g0 + min(tk, nt - 1)) * a.I;
+  down_xs<NT>(a, w, ex, g0, nt, xs);
   float2 acc[R][NT];
-  rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc);
+  rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc, primed);
 #pragma unroll
   for (int tk = 0; tk < NT; ++tk)
 #pragma unroll
@@ -484,24 +577,29 @@ __device__ void down_group(const LayerArgs& a, const DecodeWs& w, const ExpertWo
 
 template <int Q, int R, bool COMPACT>
 __device__ void down_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
-                          const pw_block_entry& ent, const PassRows<R>& pr, const SmemPtrs& s,
+                          const SlotInfo& ent, const PassRows<R>& pr, const SmemPtrs& s,
                           const BitConsts& bc) {
   __syncthreads();
   load_luts<Q, R, COMPACT>(ent.lut, pr, s);
   grid_dependency_wait();   // h is complete from here on
+  const int nt0 = min(kTG, ex.ne);
+  if (nt0 == 1) down_prime<Q, R, 1>(a, w, ex, ent, pr, 0, nt0);
+  else if (nt0 == 2) down_prime<Q, R, 2>(a, w, ex, ent, pr, 0, nt0);
+  else down_prime<Q, R, 4>(a, w, ex, ent, pr, 0, nt0);
   __syncthreads();
   for (int g0 = 0; g0 < ex.ne; g0 += kTG) {
     const int nt = min(kTG, ex.ne - g0);
-    if (nt == 1) down_group<Q, R, COMPACT, 1>(a, w, ex, ent, pr, g0, nt, s, bc);
-    else if (nt == 2) down_group<Q, R, COMPACT, 2>(a, w, ex, ent, pr, g0, nt, s, bc);
-    else down_group<Q, R, COMPACT, 4>(a, w, ex, ent, pr, g0, nt, s, bc);
+    const bool primed = (g0 == 0);
+    if (nt == 1) down_group<Q, R, COMPACT, 1>(a, w, ex, ent, pr, g0, nt, s, bc, primed);
+    else if (nt == 2) down_group<Q, R, COMPACT, 2>(a, w, ex, ent, pr, g0, nt, s, bc, primed);
+    else down_group<Q, R, COMPACT, 4>(a, w, ex, ent, pr, g0, nt, s, bc, primed);
   }
 }
 
 // A down tile of `rows` (64, or 32 on a ragged last tile) rows from n0.
 template <int Q>
 __device__ void down_tile(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
-                          const pw_block_entry& ent, int n0, int rows, const SmemPtrs& s,
+                          const SlotInfo& ent, int n0, int rows, const SmemPtrs& s,
                           const BitConsts& bc) {
   if (Q == 8 || rows == 32) {
 #pragma unroll 1
@@ -529,38 +627,47 @@ __global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArg
   // Routing (from the prep launch, which finished before the gate_up
   // kernel allowed this launch) is readable now; h only after the wait.
   const int n_routed = w.ctl[0];
+  if (n_routed == 0) {
+    // every routed expert went to the GEMM kernels (or none was routed):
+    // only the combine is left
+    grid_dependency_wait();
+    const long long total = static_cast<long long>(a.T) * a.H;
+    for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * kThreads) {
+      const int tt = static_cast<int>(i / a.H), n = static_cast<int>(i % a.H);
+      float acc = 0.f;
+      for (int j = 0; j < a.k; ++j) {
+        const int p = tt * a.k + j;
+        const int e = a.topk_ids[p];
+        if (e < 0 || e >= a.E) continue;
+        acc = fmaf(a.topk_weights[p], __ldcg(w.y + static_cast<long long>(p) * a.H + n), acc);
+      }
+      a.out[i] = acc;
+    }
+    return;
+  }
   const int tpe = (a.H + kDownRows - 1) / kDownRows;
   const int total = n_routed * tpe;
-  for (;;) {
-    const int t = next_tile(&w.ctl[2], &s.misc[0]);
+  for (bool first = true;; first = false) {
+    const int t = next_tile(&w.ctl[2], &s.misc[0], first);
     if (t >= total) break;
     const int slot = t / tpe, x = t - slot * tpe;
-    ExpertWork ex;
-    ex.e = w.routed_dn[slot];
-    ex.off = w.offsets[ex.e];
-    ex.ne = w.offsets[ex.e + 1] - ex.off;
-    const pw_block_entry gu = a.table[2 * ex.e];
-    const pw_block_entry ent = a.table[2 * ex.e + 1];
+    const SlotInfo si = w.routed_dn[slot];
+    const ExpertWork ex{si.e, si.off, si.ne};
     const int n0 = x * kDownRows;
     const int rows = min(kDownRows, a.H - n0);   // 64, or 32 on a ragged last range
-    if (gu.state != PW_PAGE_GPU || ent.state != PW_PAGE_GPU || !supported_q(gu.q) ||
-        !supported_q(ent.q)) {
+    if (si.err) {
       // this expert contributes zero; gate_up skipped it (h is not valid)
-      if (x == 0 && threadIdx.x == 0) {
-        if (gu.state != PW_PAGE_GPU || ent.state != PW_PAGE_GPU)
-          latch_status(a.status, PW_ERR_PAGE_NOT_RESIDENT);
-        else if (!supported_q(ent.q))
-          latch_status(a.status, PW_ERR_UNSUPPORTED_Q);
-      }
+      if (x == 0 && threadIdx.x == 0 && si.err > 0) latch_status(a.status, si.err);
       for (int i = threadIdx.x; i < ex.ne * rows; i += kThreads)
         w.y[static_cast<long long>(w.perm[ex.off + i / rows]) * a.H + n0 + (i % rows)] = 0.f;
     } else {
-      switch (ent.q) {
-        case 3: down_tile<3>(a, w, ex, ent, n0, rows, s, bc); break;
-        case 4: down_tile<4>(a, w, ex, ent, n0, rows, s, bc); break;
-        case 5: down_tile<5>(a, w, ex, ent, n0, rows, s, bc); break;
-        case 6: down_tile<6>(a, w, ex, ent, n0, rows, s, bc); break;
-        default: down_tile<8>(a, w, ex, ent, n0, rows, s, bc); break;
+      switch (si.q) {
+        case 3: down_tile<3>(a, w, ex, si, n0, rows, s, bc); break;
+        case 4: down_tile<4>(a, w, ex, si, n0, rows, s, bc); break;
+        case 5: down_tile<5>(a, w, ex, si, n0, rows, s, bc); break;
+        case 6: down_tile<6>(a, w, ex, si, n0, rows, s, bc); break;
+        default: down_tile<8>(a, w, ex, si, n0, rows, s, bc); break;
       }
     }
     // Arrival: the last routed expert to finish this row range combines it.
@@ -654,9 +761,10 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
     for (int ww = 0; ww < kPrepWarps; ++ww) total += s_warp_sum[ww];
     w.offsets[E] = total;
   }
-  // routed experts by bitwidth class
+  // routed experts by bitwidth class (experts the GEMM kernels take are left out)
+  const int heavy_min = w.heavy_min > 0 ? w.heavy_min : INT_MAX;
   for (int e = tid; e < E; e += kPrepThreads) {
-    if (count[e] > 0) {
+    if (count[e] > 0 && count[e] < heavy_min) {
       atomicAdd(&s_bucket[0][q_class(a.table[2 * e].q)], 1);
       atomicAdd(&s_bucket[1][q_class(a.table[2 * e + 1].q)], 1);
     }
@@ -677,9 +785,30 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
   }
   __syncthreads();
   for (int e = tid; e < E; e += kPrepThreads) {
-    if (count[e] > 0) {
-      w.routed_gu[atomicAdd(&s_bucket[0][q_class(a.table[2 * e].q)], 1)] = e;
-      w.routed_dn[atomicAdd(&s_bucket[1][q_class(a.table[2 * e + 1].q)], 1)] = e;
+    if (count[e] > 0 && count[e] < heavy_min) {
+      const pw_block_entry gu = a.table[2 * e], dn = a.table[2 * e + 1];
+      const bool gu_ok = gu.state == PW_PAGE_GPU && supported_q(gu.q);
+      const bool dn_ok = dn.state == PW_PAGE_GPU && supported_q(dn.q);
+      SlotInfo si;
+      si.e = e;
+      si.off = base[e];
+      si.ne = count[e];
+      si.pad = 0;
+      si.q = gu.q;
+      si.planes = gu.planes;
+      si.lut = gu.lut;
+      si.err = gu_ok ? PW_OK
+                     : (gu.state != PW_PAGE_GPU ? PW_ERR_PAGE_NOT_RESIDENT : PW_ERR_UNSUPPORTED_Q);
+      w.routed_gu[atomicAdd(&s_bucket[0][q_class(gu.q)], 1)] = si;
+      // down tiles of an expert whose gate_up block cannot run write zeros
+      // (their h is not valid); the error was latched by the gate_up tiles
+      si.q = dn.q;
+      si.planes = dn.planes;
+      si.lut = dn.lut;
+      si.err = !gu_ok ? -1
+               : dn_ok ? PW_OK
+                       : (dn.state != PW_PAGE_GPU ? PW_ERR_PAGE_NOT_RESIDENT : PW_ERR_UNSUPPORTED_Q);
+      w.routed_dn[atomicAdd(&s_bucket[1][q_class(dn.q)], 1)] = si;
     }
   }
   // stable placement: rank among same-expert lanes (match), earlier warps of
@@ -731,7 +860,7 @@ WsSizes ws_sizes(const pw_moe_shape& s) {
   z.y = round256(4 * P * s.H);
   z.offsets = round256(4 * (static_cast<size_t>(s.E) + 1));
   z.perm = round256(4 * P);
-  z.routed = round256(4 * static_cast<size_t>(s.E));
+  z.routed = round256(sizeof(SlotInfo) * static_cast<size_t>(s.E));
   z.ctl = 256;
   z.arrive = round256(4 * static_cast<size_t>(s.H / 32));
   return z;
@@ -764,16 +893,24 @@ cudaError_t launch_dependent(Kernel kernel, dim3 grid, dim3 block, size_t smem, 
   return cudaLaunchKernelEx(&cfg, kernel, a, w, bc);
 }
 
+// Some expert can hold kHeavyMinTokens pairs (an expert takes at most one
+// pair per token) and the GEMM kernels support the shape.
+bool hybrid_possible(const pw_moe_shape& s) {
+  return s.T >= kHeavyMinTokens && prefill_shape_ok(s);
+}
+
 }  // namespace
 
 // Workspace: x32 [T][H] | h [T*k][I] | y [T*k][H] fp32 | offsets [E+1] |
-// perm [T*k] | routed lists [E] x 2 | control words | arrival counters [H/32].
-size_t decode_workspace_bytes(const pw_moe_shape& s) {
+// perm [T*k] | routed lists [E] x 2 | control words | arrival counters [H/32]
+// | (when some expert can hold kHeavyMinTokens pairs) the GEMM kernels' scratch.
+size_t decode_workspace_bytes(const pw_moe_shape& s, bool hybrid) {
   const WsSizes z = ws_sizes(s);
-  return z.x32 + z.h + z.y + z.offsets + z.perm + 2 * z.routed + z.ctl + z.arrive;
+  const size_t base = z.x32 + z.h + z.y + z.offsets + z.perm + 2 * z.routed + z.ctl + z.arrive;
+  return base + ((hybrid && hybrid_possible(s)) ? heavy_scratch_bytes(s) : 0);
 }
 
-cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream) {
+cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, bool hybrid) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel,
@@ -796,10 +933,12 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream) {
   w.y = reinterpret_cast<float*>(p); p += z.y;
   w.offsets = reinterpret_cast<int*>(p); p += z.offsets;
   w.perm = reinterpret_cast<int*>(p); p += z.perm;
-  w.routed_gu = reinterpret_cast<int*>(p); p += z.routed;
-  w.routed_dn = reinterpret_cast<int*>(p); p += z.routed;
+  w.routed_gu = reinterpret_cast<SlotInfo*>(p); p += z.routed;
+  w.routed_dn = reinterpret_cast<SlotInfo*>(p); p += z.routed;
   w.ctl = reinterpret_cast<int*>(p); p += z.ctl;
-  w.arrive = reinterpret_cast<int*>(p);
+  w.arrive = reinterpret_cast<int*>(p); p += z.arrive;
+  const bool heavy = hybrid && hybrid_possible(shape);
+  w.heavy_min = heavy ? kHeavyMinTokens : 0;
 
   const size_t prep_smem = sizeof(int) * static_cast<size_t>(a.E) * (2 + kPrepWarps);
   if (prep_smem > 48 * 1024) {
@@ -814,6 +953,10 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream) {
   decode_prep_kernel<<<prep_grid, kPrepThreads, prep_smem, stream>>>(a, w);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (heavy) {
+    e = launch_heavy(a, w.offsets, w.perm, w.y, p, kHeavyMinTokens, stream);
+    if (e != cudaSuccess) return e;
+  }
 
   const int slots = a.E < n_pairs ? a.E : n_pairs;
   const int resident = 2 * sm_count();

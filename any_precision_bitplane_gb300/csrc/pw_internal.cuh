@@ -65,8 +65,14 @@ struct LayerArgs {
   float* out;                    // [T][H]
   int32_t* status;
 };
-size_t decode_workspace_bytes(const pw_moe_shape& s);
-cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t s);
+// Experts with at least this many pairs in a decode call go through the
+// tensor-core GEMM kernels of the prefill path (when the shape allows it);
+// the others through the decode kernels.
+constexpr int kHeavyMinTokens = 16;
+// `hybrid` = false keeps every expert on the decode kernels (and the
+// workspace free of the GEMM path's buffers).
+size_t decode_workspace_bytes(const pw_moe_shape& s, bool hybrid = true);
+cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t s, bool hybrid = true);
 int decode_max_pairs();
 int decode_max_experts();
 
@@ -75,5 +81,11 @@ size_t prefill_workspace_bytes(const pw_moe_shape& s);
 cudaError_t launch_prefill(const LayerArgs& a, void* ws, cudaStream_t s);
 int prefill_min_pairs(const pw_moe_shape& s);
 bool prefill_shape_ok(const pw_moe_shape& s);  // H % 128 == 0, I % 64 == 0, E <= 1024
+// The GEMM kernels of the prefill path over the experts that hold at least
+// min_tokens pairs, on a grouping (offsets, perm) made by the caller; writes
+// y[pair][H] of those pairs.  Scratch: heavy_scratch_bytes(s).
+size_t heavy_scratch_bytes(const pw_moe_shape& s);
+cudaError_t launch_heavy(const LayerArgs& a, const int32_t* offsets, const int32_t* perm, float* y,
+                         void* scratch, int min_tokens, cudaStream_t s);
 
 }  // namespace pw

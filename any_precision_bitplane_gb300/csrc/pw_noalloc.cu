@@ -75,7 +75,7 @@ extern "C" int pw_moe_forward_noalloc(const pw_moe_shape* shape, const void* hid
   if (n_pairs > pw::decode_max_pairs() || s.E > pw::decode_max_experts())
     return fail(PW_ERR_SHAPE, "decode path limits: T*k <= %d, E <= %d", pw::decode_max_pairs(),
                 pw::decode_max_experts());
-  const size_t need = pw::decode_workspace_bytes(s);
+  const size_t need = pw::decode_workspace_bytes(s, false);
   if (need > pw::kStaticScratchBytes)
     return fail(PW_ERR_WORKSPACE,
                 "shape needs %zu bytes of scratch; the static scratch of "
@@ -106,7 +106,7 @@ extern "C" int pw_moe_forward_noalloc(const pw_moe_shape* shape, const void* hid
   a.table = table->d_entries;
   a.out = out;
   a.status = table->d_status;
-  e = pw::launch_decode(a, scratch, stream);
+  e = pw::launch_decode(a, scratch, stream, false);
   if (e != cudaSuccess) return pw::cuda_fail(e, "forward launch");
   return PW_OK;
 }

@@ -124,6 +124,7 @@ struct GemmArgs {
   __half* h_ws;             // [n_pairs][I] (gate_up writes, down reads through TMA)
   float* y_ws;              // [n_pairs][H]
   int32_t* tile_counter;    // zeroed by the gather launch
+  int32_t min_tokens;       // experts with fewer pairs get no tiles
   int32_t* status;
 };
 
@@ -570,7 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = 0;
     for (int e = 0; e < a.E; ++e) {
       prefix[e] = run;
-      run += mt * ((a.offsets[e + 1] - a.offsets[e] + BN - 1) / BN);
+      const int cnt = a.offsets[e + 1] - a.offsets[e];
+      if (cnt >= a.min_tokens) run += mt * ((cnt + BN - 1) / BN);
     }
     prefix[a.E] = run;
     for (int i = 0; i < NST; ++i) {
@@ -928,6 +930,68 @@ int num_sms() {
 
 }  // namespace
 
+size_t heavy_scratch_bytes(const pw_moe_shape& s) {
+  const size_t P = static_cast<size_t>(s.T) * s.k;
+  return 256 + round256(2 * P * s.H) + round256(2 * P * s.I);
+}
+
+// Decode calls with experts that hold many pairs: those experts run through
+// the gather and the two GEMM kernels here, on the decode path's grouping,
+// and write their pairs' rows of y; the decode kernels take the rest and
+// combine.
+cudaError_t launch_heavy(const LayerArgs& la, const int32_t* offsets, const int32_t* perm, float* y,
+                         void* scratch, int min_tokens, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(dq_gemm_kernel<kGateUp>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dq_gemm_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int n_pairs = la.T * la.k;
+  const size_t P = static_cast<size_t>(n_pairs);
+  char* p = static_cast<char*>(scratch);
+  int32_t* counters = reinterpret_cast<int32_t*>(p);
+  p += 256;
+  __half* xg = reinterpret_cast<__half*>(p);
+  p += round256(2 * P * la.H);
+  __half* h = reinterpret_cast<__half*>(p);
+  const long long gwork = static_cast<long long>(n_pairs) * (la.H / 8);
+  const int gblocks = static_cast<int>(std::min<long long>((gwork + 255) / 256, 152LL * 32));
+  gather_kernel<<<gblocks, 256, 0, stream>>>(la.hidden, perm, offsets, la.E, la.k, la.H, n_pairs, xg,
+                                             counters);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap map_x, map_h;
+  if (!make_map(&map_x, xg, n_pairs, la.H) || !make_map(&map_h, h, n_pairs, la.I))
+    return cudaErrorInvalidValue;
+  GemmArgs g;
+  g.H = la.H;
+  g.I = la.I;
+  g.E = la.E;
+  g.k = la.k;
+  g.n_pairs = n_pairs;
+  g.table = la.table;
+  g.offsets = offsets;
+  g.perm = perm;
+  g.h_ws = h;
+  g.y_ws = y;
+  g.status = la.status;
+  g.min_tokens = min_tokens;
+  const int grid = num_sms();
+  const BitConsts bc = make_bit_consts();
+  g.tile_counter = counters;
+  dq_gemm_kernel<kGateUp><<<grid, kThreads, kSmemBytes, stream>>>(g, map_x, bc);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  g.tile_counter = counters + 1;
+  dq_gemm_kernel<kDown><<<grid, kThreads, kSmemBytes, stream>>>(g, map_h, bc);
+  return cudaGetLastError();
+}
+
 size_t prefill_workspace_bytes(const pw_moe_shape& s) {
   const size_t P = static_cast<size_t>(s.T) * s.k;
   return 256 + round256(sizeof(int32_t) * (s.E + 1)) + round256(sizeof(int32_t) * P) +
@@ -980,6 +1044,7 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   g.h_ws = w.h;
   g.y_ws = w.y;
   g.status = la.status;
+  g.min_tokens = 1;
   const int grid = num_sms();
   const BitConsts bc = make_bit_consts();
   g.tile_counter = w.counters;

@@ -71,7 +71,9 @@ extern "C" {
 
 /* ---- forward paths ----------------------------------------------------- */
 #define PW_PATH_AUTO     0  /* decode kernels for small token counts, else prefill */
-#define PW_PATH_DECODE   1  /* CUDA-core fused decode kernels                       */
+#define PW_PATH_DECODE   1  /* CUDA-core fused decode kernels; within a call, experts
+                                holding >= 16 pairs go through the tcgen05 GEMM
+                                kernels (when the shape allows them)               */
 #define PW_PATH_PREFILL  2  /* dequantise-to-shared-memory tcgen05 GEMM kernels     */
 
 /* One linear block's page-table entry (24 bytes).  PagedWeight, "Core
@@ -243,7 +245,7 @@ int32_t pw_prefill_min_pairs(const pw_moe_shape* shape);
  * workspace: the scratch lives in one static device array of 8 MiB inside
  * libpw (every GPU that loads the library keeps those 8 MiB until the process
  * exits).  The caller still passes inputs and outputs.
- *   - Shapes whose decode scratch, about 4*T*H + 4*T*k*(I + H + 1) + 12*E
+ *   - Shapes whose decode scratch, about 4*T*H + 4*T*k*(I + H + 1) + 84*E
  *     + H/8 bytes (each section rounded up to 256 bytes), exceeds 8 MiB are
  *     rejected with
  *     PW_ERR_WORKSPACE (use pw_moe_forward with a workspace instead), as
