@@ -20,11 +20,12 @@
 //               publishes each through a 4-deep ring in shared memory, and
 //               TMA-loads the fp16 token rows (64-byte swizzle) of every k-step.
 //   warp 21     plane producer: per k-step (32 columns = one plane word
-//               column), bulk-copies the words of the tile's 128 rows from
-//               each of the top q planes into a 6-deep ring (a word column of
+//               column), copies the words of the tile's 128 rows from each
+//               of the top q planes into a 6-deep ring (a word column of
 //               consecutive rows is contiguous: two 256-byte runs for a
-//               gate_up tile, one 512-byte run for a down tile), one copy
-//               per lane so that the copies of a k-step start together.
+//               gate_up tile, one 512-byte run for a down tile) with 16-byte
+//               cp.async per lane, whose completion arrives on the stage's
+//               barrier; the copy engine stays free for the token operand.
 //   warps 0-15  dequant: two sets of eight that take alternate k-steps.  In a
 //               set, four warps own columns 0-15 of the k-step and four own
 //               columns 16-31; each thread owns one A row.  A thread reads
@@ -251,13 +252,14 @@ __device__ __forceinline__ void named_sync_epi() {
   asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// The barrier receives one arrival when all of this thread's earlier
+// cp.async copies have landed (its expected count includes that arrival).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
@@ -581,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_base + 8 * (kBarEmpty + i), 1);
     }
     for (int i = 0; i < NPS; ++i) {
-      mbar_init(bar_base + 8 * (kBarPlFull + i), 1);
+      mbar_init(bar_base + 8 * (kBarPlFull + i), 32);
       mbar_init(bar_base + 8 * (kBarPlEmpty + i), kSetThreads);
     }
     for (int i = 0; i < kTileRing; ++i) {
@@ -726,23 +728,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t full = bar_base + 8 * (kBarPlFull + ps);
-          const uint32_t dst = sbase + kOffPlanes + ps * kPlaneStage;
-          if (lane == 0) mbar_arrive_tx(full, static_cast<uint32_t>(q) * 512u);
-          __syncwarp();
-          const uint32_t* col = base + static_cast<long long>(s) * N;
-          if (mode == kGateUp) {
-            if (lane < 2 * q) {   // lane 2p + seg: plane p, gate (0) or up (1) run
-              const int p = lane >> 1, seg = lane & 1;
-              bulk_copy(dst + p * 512 + seg * 256, col + p * plane_stride + (seg ? a.I : 0), 256,
-                        full);
-            }
-          } else if (lane < q) {
-            bulk_copy(dst + lane * 512, col + lane * plane_stride, 512, full);
-          }
+          const uint32_t dst = sbase + kOffPlanes + ps * kPlaneStage + lane * 16;
+          // lane L copies 16 bytes of each plane: words 4L..4L+3 of the
+          // stage slab (gate_up: lanes 0-15 the gate run, 16-31 the up run)
+          const uint32_t* src = base + static_cast<long long>(s) * N +
+                                ((mode == kGateUp) ? ((lane >> 4) * a.I + (lane & 15) * 4) : lane * 4);
+          for (int p = 0; p < q; ++p) cp_async16(dst + p * 512, src + p * plane_stride);
+          cp_async_arrive(full);
         }
         if (!ok) break;
       }
-      if (*abort && lane == 0) drain_copies(bar_base, kBarPlFull, NPS, pit, NPS);
+      asm volatile("cp.async.wait_all;" ::: "memory");   // nothing in flight at exit
     }
   } else {
     // ---- MMA issuer
