@@ -74,6 +74,7 @@ _SIGNATURES = {
     "pw_moe_forward_path": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _c.c_size_t, _I32, _P]),
     "pw_prefill_min_pairs": (_I32, [_P]),
     "pw_moe_forward_noalloc": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P]),
+    "pw_set_timing_events": (_c.c_int, [_P, _P]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -288,3 +289,12 @@ def moe_forward_noalloc(hidden, topk_ids, topk_weights, table, I, E, out=None, s
                                         _ptr(topk_weights), table.handle, _ptr(out),
                                         _stream(stream)), "pw_moe_forward_noalloc")
     return out
+
+
+def set_timing_events(before=None, after=None):
+    """Record torch.cuda.Event `before` / `after` (timing enabled, already
+    recorded once so that they exist) around the dominant kernel of every
+    following forward call; None, None stops."""
+    b = before.cuda_event if before is not None else None
+    a = after.cuda_event if after is not None else None
+    _check(lib().pw_set_timing_events(b, a), "pw_set_timing_events")

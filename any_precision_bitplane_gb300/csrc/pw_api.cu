@@ -7,6 +7,18 @@
 #include "pw_internal.cuh"
 
 namespace pw {
+
+TimingEvents g_timing;
+
+cudaError_t record_timing(cudaEvent_t ev, cudaStream_t s) {
+  if (ev == nullptr) return cudaSuccess;
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &st);
+  if (e != cudaSuccess) return e;
+  return st == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                             : cudaEventRecord(ev, s);
+}
+
 namespace {
 thread_local char g_err[512] = "";
 
@@ -161,6 +173,14 @@ extern "C" {
 const char* pw_last_error(void) { return pw::g_err; }
 
 int pw_version(void) { return 100; }
+
+int pw_set_timing_events(cudaEvent_t before, cudaEvent_t after) {
+  if ((before == nullptr) != (after == nullptr))
+    return fail(PW_ERR_INVALID_ARG, "pass both events or neither");
+  pw::g_timing.before = before;
+  pw::g_timing.after = after;
+  return PW_OK;
+}
 
 int pw_pack_bitplanes(const uint8_t* codes, int32_t N, int32_t K, uint32_t* planes,
                       cudaStream_t stream) {

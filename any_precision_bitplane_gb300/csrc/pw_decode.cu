@@ -963,9 +963,11 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
   const int gu_tiles = slots * (a.I / kPairsPerTile);
   const int dn_tiles = slots * ((a.H + kDownRows - 1) / kDownRows);
   const BitConsts bc = make_bit_consts();
+  if ((e = record_timing(g_timing.before, stream)) != cudaSuccess) return e;
   e = launch_dependent(decode_gateup_kernel, dim3(gu_tiles < resident ? gu_tiles : resident),
                        dim3(kThreads), kSmemBytes, stream, a, w, bc);
   if (e != cudaSuccess) return e;
+  if ((e = record_timing(g_timing.after, stream)) != cudaSuccess) return e;
   return launch_dependent(decode_down_kernel, dim3(dn_tiles < resident ? dn_tiles : resident),
                           dim3(kThreads), kSmemBytes, stream, a, w, bc);
 }

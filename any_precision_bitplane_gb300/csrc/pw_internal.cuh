@@ -55,6 +55,15 @@ struct CommitBatch {
 };
 cudaError_t launch_commit(pw_block_entry* entries, const CommitBatch& batch, cudaStream_t s);
 
+// Measurement hook (pw_set_timing_events): events recorded around the
+// dominant kernel of each forward call; record_timing is a no-op for NULL.
+struct TimingEvents {
+  cudaEvent_t before = nullptr;
+  cudaEvent_t after = nullptr;
+};
+extern TimingEvents g_timing;
+cudaError_t record_timing(cudaEvent_t ev, cudaStream_t s);
+
 // Fused layer, decode path.
 struct LayerArgs {
   int32_t T, H, I, E, k;

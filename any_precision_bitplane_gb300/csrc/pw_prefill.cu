@@ -1044,8 +1044,10 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   const int grid = num_sms();
   const BitConsts bc = make_bit_consts();
   g.tile_counter = w.counters;
+  if ((e = record_timing(g_timing.before, stream)) != cudaSuccess) return e;
   dq_gemm_kernel<kGateUp><<<grid, kThreads, kSmemBytes, stream>>>(g, map_x, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = record_timing(g_timing.after, stream)) != cudaSuccess) return e;
   g.tile_counter = w.counters + 1;
   dq_gemm_kernel<kDown><<<grid, kThreads, kSmemBytes, stream>>>(g, map_h, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

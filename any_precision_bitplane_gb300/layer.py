@@ -76,12 +76,14 @@ class DeviceLayer:
         c.table = PageTable(c.entries())
         return c
 
-    def routed_bytes(self, topk_ids_np):
+    def routed_bytes(self, topk_ids_np, blocks=(0, 1)):
         """Algorithmic weight bytes one forward call reads: top-q planes + committed LUT
-        of every block of every routed expert."""
+        of every block of every routed expert (blocks: 0 = gate_up, 1 = down)."""
         total = 0
         for e in np.unique(np.asarray(topk_ids_np)):
             for m, (N, K) in enumerate(((2 * self.I, self.H), (self.H, self.I))):
+                if m not in blocks:
+                    continue
                 q = int(self.q[e, m])
                 total += q * N * K // 8 + N * (1 << q) * 2
         return total

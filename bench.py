@@ -95,17 +95,18 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload, T):
-    """DRAM bytes per forward call from the committed ncu summary, if it was
-    taken on the current kernel sources; else None."""
+def recorded_traffic(kernel, workload, T):
+    """DRAM bytes (read + write) per launch of `kernel` on this workload from
+    the committed ncu summary, if it was taken on the current kernel sources;
+    else None.  Line format: kernel workload T=<T> <bytes> <source sha>."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     try:
         with open(path) as f:
             for line in f:
                 parts = line.split()
-                if len(parts) == 4 and parts[0] == workload and parts[1] == "T=%d" % T:
-                    if parts[3] == kernel_source_sha():
-                        return float(parts[2])
+                if (len(parts) == 5 and parts[0] == kernel and parts[1] == workload
+                        and parts[2] == "T=%d" % T and parts[4] == kernel_source_sha()):
+                    return float(parts[3])
     except OSError:
         pass
     return None
@@ -222,6 +223,40 @@ def time_device(pw, cfg, layers, hidden, ids, wts, steps, warmup, stream):
         return g, start, stop, out
 
 
+def time_dominant(pw, cfg, layers, hidden, ids, wts, steps, stream):
+    """Average duration of the call's dominant kernel: the library records a
+    pair of CUDA events around it (on the launching stream) in every step of
+    a captured graph of `steps` calls; returns milliseconds per launch."""
+    import torch
+    T = hidden.shape[0]
+    out = torch.empty((T, cfg.H), dtype=torch.float32, device=hidden.device)
+    ws = torch.empty(max(pw.workspace_bytes(T, cfg.H, cfg.I, cfg.E, cfg.k), 256),
+                     dtype=torch.uint8, device=hidden.device)
+    L = len(layers)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for b, a in evs:        # create the events before capture
+            b.record(stream)
+            a.record(stream)
+        pw.moe_forward(hidden, ids, wts, layers[0].table, cfg.I, cfg.E, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(steps):
+                    pw.set_timing_events(*evs[i])
+                    pw.moe_forward(hidden, ids, wts, layers[i % L].table, cfg.I, cfg.E, out=out,
+                                   workspace=ws)
+        finally:
+            pw.set_timing_events(None, None)
+        g.replay()
+        torch.cuda.synchronize()
+    total = sum(b.elapsed_time(a) for b, a in evs)
+    del g
+    return total / steps
+
+
 def time_e2e(pw, cfg, layers, host, steps, warmup, device):
     """Through the public API with host buffers: per step, H2D of the step's
     inputs from pinned memory, the forward call, D2H of the output."""
@@ -296,6 +331,50 @@ def cpu_baseline(name, T, budget_s=20.0):
                       "blocks encoded before timing)" % (calls, T)}
 
 
+def hidden_bytes(cfg, T):
+    """bf16 hidden states of one batch."""
+    return T * cfg.H * 2
+
+
+def decode_config(pw, name, T, device, stream, steps, warmup, recommit=False):
+    """Tokens/s and achieved bytes/s of another decode workload (same timing
+    method as the headline; a parity-test configuration, reported as context)."""
+    import torch
+    from workloads import gen
+    cfg, layer, layers, hidden, ids, wts, step_bytes, weight_bytes, _ = \
+        setup_workload(name, T, device)
+    peak, _ = measured_peaks()
+    res = {}
+    phases = ["before recommit", "after recommit"] if recommit else [""]
+    for ph in phases:
+        if ph == "after recommit":
+            blocks, new_q = gen.make_recommit(layer)
+            for x in layers:
+                x.commit(blocks, new_q)
+            torch.cuda.synchronize()
+            step_bytes = (layers[0].routed_bytes(ids.cpu().numpy()) + T * cfg.H * 2 +
+                          T * cfg.k * 8 + T * cfg.H * 4)
+        g, s0, s1, _ = time_device(pw, cfg, layers, hidden, ids, wts, steps, warmup, stream)
+        with torch.cuda.stream(stream):
+            s0.record(stream)
+            g.replay()
+            s1.record(stream)
+        torch.cuda.synchronize()
+        ms = s0.elapsed_time(s1)
+        gbs = step_bytes / (ms / 1e3 / steps) / 1e9
+        entry = {"tokens_per_s": T * steps / (ms / 1e3), "us_per_step": ms * 1e3 / steps,
+                 "GB_per_s": gbs, "frac": gbs / peak, "bytes_per_step": step_bytes}
+        if ph:
+            res[ph] = entry
+        else:
+            res = entry
+        del g
+    for x in layers:
+        x.close()
+    torch.cuda.empty_cache()
+    return res
+
+
 def prefill_section(pw, device, steps=5, warmup=2, tokens=0):
     """Mixtral-shaped prefill (4096 tokens, top-2 of 8 experts, H=4096,
     I=14336): the dequantise-to-shared-memory tcgen05 path."""
@@ -326,17 +405,28 @@ def prefill_section(pw, device, steps=5, warmup=2, tokens=0):
     flops = 2.0 * T * cfg.k * (cfg.H * 2 * cfg.I + cfg.I * cfg.H)
     peak, kind = tensor_peak()
     tflops = flops / (ms / 1e3) / 1e12
+    # the dominant kernel (gate_up dequant-GEMM), timed with events around its launches
+    stream = torch.cuda.Stream(device)
+    gu_ms = time_dominant(pw, cfg, [dl], hidden, ids, wts, steps, stream)
+    gu_flops = 2.0 * T * cfg.k * cfg.H * 2 * cfg.I
+    gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12
     dl.close()
     del ws
     torch.cuda.empty_cache()
     return {"workload": "%s: H=%d I=%d E=%d top-%d, T=%d" % (cfg.name, cfg.H, cfg.I, cfg.E,
                                                             cfg.k, T),
             "tokens_per_s": T / (ms / 1e3), "ms_per_step": ms, "steps": steps,
-            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
-                         "unit": "TFLOP/s", "frac": tflops / peak, "peak_kind": kind,
-                         "flops_per_step": flops,
-                         "kernel": "whole prefill call (permute, gather, gate_up and down "
-                                   "dequant+tcgen05 GEMMs, combine)"}}
+            "roofline": {"bound": "tensor", "achieved": gu_tflops, "peak": peak,
+                         "unit": "TFLOP/s", "frac": gu_tflops / peak, "peak_kind": kind,
+                         "flops_per_launch": gu_flops, "ms_per_launch": gu_ms,
+                         "kernel": "dq_gemm_kernel<gate_up> (dequant + tcgen05 GEMM + SiLU; "
+                                   "the call's largest launch)",
+                         "traffic": recorded_traffic("dq_gemm_kernel<0>", cfg.name, T)},
+            "call_roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
+                              "unit": "TFLOP/s", "frac": tflops / peak,
+                              "flops_per_call": flops,
+                              "kernel": "whole prefill call (permute, gather, gate_up and down "
+                                        "dequant+tcgen05 GEMMs, combine)"}}
 
 
 def native(args):
@@ -391,6 +481,13 @@ def native(args):
     per_launch_s = ms / 1e3 / args.steps
     achieved = step_bytes / per_launch_s / 1e9
 
+    # dominant kernel (decode gate_up): its own launches timed with events
+    dom_ms = time_dominant(pw, cfg, layers, hidden, ids, wts, args.steps, stream)
+    ids_np = ids.cpu().numpy()
+    gu_bytes = (layers[0].routed_bytes(ids_np, blocks=(0,)) + hidden_bytes(cfg, args.T) +
+                args.T * cfg.k * cfg.I * 4)
+    dom_achieved = gu_bytes / (dom_ms / 1e3) / 1e9
+
     e2e = None
     if not args.no_e2e:
         e2e_dt, bi, bo = time_e2e(pw, cfg, layers, host, args.steps, args.warmup, device)
@@ -422,7 +519,12 @@ def native(args):
             torch.cuda.empty_cache()
 
     prefill = None
+    configs_out = {}
     if not args.no_sweep and rank == 0 and world == 1:
+        configs_out["mixtral_decode T=4"] = decode_config(pw, "mixtral_decode", 4, device, stream,
+                                                          args.steps, args.warmup)
+        configs_out["qwen3_decode T=64"] = decode_config(pw, "qwen3_decode", 64, device, stream,
+                                                         args.steps, args.warmup, recommit=True)
         prefill = prefill_section(pw, device)
 
     clocks = sampler.summary(w0, w1)
@@ -446,18 +548,24 @@ def native(args):
                          "weights per step" % (len(layers), weight_bytes / 1e6),
                    "timing": "CUDA events around one CUDA-graph replay of exactly K steps",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "pw_moe_forward decode call (3 launches: hidden->fp32, "
-                               "gate_up+SiLU, down+combine)",
-                     "bytes_per_launch": step_bytes,
-                     "traffic": recorded_traffic(args.workload, T)},
+        "roofline": {"bound": "hbm", "achieved": dom_achieved, "peak": peak, "unit": "GB/s",
+                     "frac": dom_achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "decode_gateup_kernel (gate_up + SiLU; the call's largest launch)",
+                     "bytes_per_launch": gu_bytes, "ms_per_launch": dom_ms,
+                     "traffic": recorded_traffic("decode_gateup_kernel", args.workload, T)},
+        "call_roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                          "frac": achieved / peak,
+                          "kernel": "whole pw_moe_forward decode call (prep, gate_up, down "
+                                    "+ combine)",
+                          "bytes_per_call": step_bytes},
         "e2e": e2e,
         "gpu_launches": DECODE_LAUNCHES_PER_CALL * args.steps,
         "clocks": clocks,
     }
     if sweep:
         line["sweep"] = sweep
+    if configs_out:
+        line["configs"] = configs_out
     if prefill is not None:
         line["prefill"] = prefill
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -234,6 +234,17 @@ int pw_moe_forward_path(const pw_moe_shape* shape, const void* hidden, const int
  * (T*k pairs >= this value). */
 int32_t pw_prefill_min_pairs(const pw_moe_shape* shape);
 
+/* ---- measurement hook ---------------------------------------------------------
+ * No counterpart on the PagedWeight pages: a benchmark needs the duration of
+ * the call's dominant kernel, which the caller cannot bracket from outside.
+ * While set, every forward call records `before` on its stream right before
+ * it launches its dominant kernel and `after` right after it: the decode
+ * path's gate_up kernel, the prefill path's gate_up GEMM.  During stream
+ * capture the records become external event-record nodes of the graph.
+ * The events must have timing enabled; pass NULL, NULL to stop.  Process-wide
+ * and not thread-safe.  Errors: PW_ERR_INVALID_ARG (exactly one is NULL). */
+int pw_set_timing_events(cudaEvent_t before, cudaEvent_t after);
+
 /* ---- the fused layer without a workspace ------------------------------------
  * The PagedWeight pages have no counterpart to this entry point; it is a
  * service for callers that cannot allocate device memory: a plugin whose
