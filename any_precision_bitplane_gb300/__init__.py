@@ -75,6 +75,11 @@ _SIGNATURES = {
     "pw_prefill_min_pairs": (_I32, [_P]),
     "pw_moe_forward_noalloc": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P]),
     "pw_set_timing_events": (_c.c_int, [_P, _P]),
+    "pw_page_table_set_routing_stats": (_c.c_int, [_P, _P, _P]),
+    "pw_planes_to_host": (_c.c_int, [_P, _I32, _I32, _I32, _P, _P]),
+    "pw_planes_from_host": (_c.c_int, [_P, _P, _I32, _I32, _I32, _P]),
+    "pw_page_table_commit_after": (_c.c_int, [_P, _I32, _P, _P, _P, _P, _P]),
+    "pw_plan_recommit": (_c.c_int, [_I32, _P, _P, _P, _P, _I32, _c.c_int64, _P, _P, _P, _P]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -201,6 +206,16 @@ class PageTable:
         _check(lib().pw_page_table_commit(self.handle, n, ids, qs, luts, _stream(stream)),
                "pw_page_table_commit")
 
+    def commit_after(self, block_ids, new_q, new_lut_ptrs, ready, stream=None):
+        """commit() ordered after torch.cuda.Event `ready` (e.g. a page reload)."""
+        n = len(block_ids)
+        ids = (ctypes.c_int32 * max(n, 1))(*[int(b) for b in block_ids])
+        qs = (ctypes.c_int32 * max(n, 1))(*[int(q) for q in new_q])
+        luts = (ctypes.c_void_p * max(n, 1))(*[int(p) for p in new_lut_ptrs])
+        _check(lib().pw_page_table_commit_after(self.handle, n, ids, qs, luts,
+                                                ctypes.c_void_p(ready.cuda_event), _stream(stream)),
+               "pw_page_table_commit_after")
+
     def set_pages(self, block_ids, planes_ptrs, states, stream=None):
         n = len(block_ids)
         ids = (ctypes.c_int32 * max(n, 1))(*[int(b) for b in block_ids])
@@ -219,6 +234,16 @@ class PageTable:
         _check(lib().pw_page_table_status(self.handle, ctypes.byref(v), 1 if reset else 0,
                                           _stream(stream)), "pw_page_table_status")
         return v.value
+
+    def set_routing_stats(self, counts=None, mass=None):
+        """Accumulate per-expert routing statistics into `counts` (int32 [E]) and
+        `mass` (float32 [E]) during every following forward call; None stops."""
+        if counts is not None:
+            _need_cuda(counts, mass)
+        self._stats = (counts, mass)   # keep the buffers alive while attached
+        _check(lib().pw_page_table_set_routing_stats(
+            self.handle, _ptr(counts) if counts is not None else None,
+            _ptr(mass) if mass is not None else None), "pw_page_table_set_routing_stats")
 
     def close(self):
         if self.handle is not None and self.handle.value:
@@ -298,3 +323,41 @@ def set_timing_events(before=None, after=None):
     b = before.cuda_event if before is not None else None
     a = after.cuda_event if after is not None else None
     _check(lib().pw_set_timing_events(b, a), "pw_set_timing_events")
+
+
+def plan_recommit(q_now, sensitivity, bytes_per_bit, routing_mass, hot_floor, bytes_to_free):
+    """Greedy damage-per-byte planner (host computation in libpw).  Arrays are
+    host sequences of length 2E (routing_mass: E).  Returns (block ids,
+    new bitwidths, bytes freed): the list a PageTable.commit applies."""
+    import numpy as np
+    q = np.ascontiguousarray(q_now, dtype=np.int32)
+    s = np.ascontiguousarray(sensitivity, dtype=np.float32)
+    b = np.ascontiguousarray(bytes_per_bit, dtype=np.int64)
+    m = np.ascontiguousarray(routing_mass, dtype=np.float32)
+    n = q.size
+    ids = np.zeros(max(n, 1), dtype=np.int32)
+    qs = np.zeros(max(n, 1), dtype=np.int32)
+    n_out = ctypes.c_int32(0)
+    freed = ctypes.c_int64(0)
+    _check(lib().pw_plan_recommit(n, q.ctypes.data, s.ctypes.data, b.ctypes.data, m.ctypes.data,
+                                  int(hot_floor), int(bytes_to_free), ids.ctypes.data,
+                                  qs.ctypes.data, ctypes.byref(n_out), ctypes.byref(freed)),
+           "pw_plan_recommit")
+    k = n_out.value
+    return ids[:k].tolist(), qs[:k].tolist(), freed.value
+
+
+def planes_to_host(planes, N, K, p_begin, host, stream=None):
+    """Copy planes [p_begin, 8) of a block (device tensor viewed as uint32
+    [8][K/32][N]) into `host` (pinned CPU tensor of (8-p_begin)*N*K/8 bytes),
+    asynchronously on `stream`."""
+    _need_cuda(planes)
+    _check(lib().pw_planes_to_host(_ptr(planes), N, K, p_begin, ctypes.c_void_p(host.data_ptr()),
+                                   _stream(stream)), "pw_planes_to_host")
+
+
+def planes_from_host(host, planes, N, K, p_begin, stream=None):
+    """Copy `host` back into planes [p_begin, 8) of a block, asynchronously."""
+    _need_cuda(planes)
+    _check(lib().pw_planes_from_host(ctypes.c_void_p(host.data_ptr()), _ptr(planes), N, K, p_begin,
+                                     _stream(stream)), "pw_planes_from_host")

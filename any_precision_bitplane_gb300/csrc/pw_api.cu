@@ -95,6 +95,8 @@ int forward_impl(const pw_moe_shape* shape, const void* hidden, const int32_t* t
   a.table = table->d_entries;
   a.out = out;
   a.status = table->d_status;
+  a.stats_counts = table->stats_counts;
+  a.stats_mass = table->stats_mass;
   cudaError_t e;
   if (path == PW_PATH_DECODE) {
     if (n_pairs > decode_max_pairs() || s.E > decode_max_experts())
@@ -270,6 +272,15 @@ int pw_page_table_create(int32_t num_blocks, const pw_block_entry* host_init,
   return PW_OK;
 }
 
+int pw_page_table_set_routing_stats(pw_page_table* t, int32_t* counts, float* mass) {
+  if (t == nullptr) return fail(PW_ERR_INVALID_ARG, "table is NULL");
+  if ((counts == nullptr) != (mass == nullptr))
+    return fail(PW_ERR_INVALID_ARG, "pass both statistics buffers or neither");
+  t->stats_counts = counts;
+  t->stats_mass = mass;
+  return PW_OK;
+}
+
 int pw_page_table_destroy(pw_page_table* t) {
   if (t == nullptr) return PW_OK;
   cudaError_t e = cudaDeviceSynchronize();
@@ -291,6 +302,57 @@ int pw_page_table_set_pages(pw_page_table* t, int32_t n, const int32_t* block_id
                             cudaStream_t stream) {
   return pw::update_table(t, n, block_ids, 1, states, reinterpret_cast<const void* const*>(planes),
                           stream);
+}
+
+int pw_page_table_commit_after(pw_page_table* t, int32_t n, const int32_t* block_ids,
+                               const int32_t* new_q, const uint16_t* const* new_lut,
+                               cudaEvent_t ready, cudaStream_t stream) {
+  if (ready != nullptr) {
+    cudaError_t e = cudaStreamWaitEvent(stream, ready, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "wait for the page copy");
+  }
+  return pw_page_table_commit(t, n, block_ids, new_q, new_lut, stream);
+}
+
+namespace pw {
+namespace {
+
+int plane_tail_args(const void* dev, const void* host, int32_t N, int32_t K, int32_t p_begin,
+                    size_t* bytes, size_t* offset) {
+  if (N < 0) return fail(PW_ERR_INVALID_ARG, "N < 0");
+  if (K <= 0 || K % 32) return fail(PW_ERR_SHAPE, "K (%d) must be a positive multiple of 32", K);
+  if (p_begin < 0 || p_begin > 7) return fail(PW_ERR_INVALID_ARG, "p_begin %d outside 0..7", p_begin);
+  if (!dev || !host || !aligned(dev, 16))
+    return fail(PW_ERR_INVALID_ARG, "NULL pointer or planes not 16-byte aligned");
+  const size_t plane = static_cast<size_t>(N) * (K / 32) * 4;
+  *bytes = plane * static_cast<size_t>(8 - p_begin);
+  *offset = plane * static_cast<size_t>(p_begin);
+  return PW_OK;
+}
+
+}  // namespace
+}  // namespace pw
+
+int pw_planes_to_host(const uint32_t* planes, int32_t N, int32_t K, int32_t p_begin, void* host,
+                      cudaStream_t stream) {
+  size_t bytes = 0, off = 0;
+  int rc = pw::plane_tail_args(planes, host, N, K, p_begin, &bytes, &off);
+  if (rc) return rc;
+  if (bytes == 0) return PW_OK;
+  cudaError_t e = cudaMemcpyAsync(host, reinterpret_cast<const char*>(planes) + off, bytes,
+                                  cudaMemcpyDeviceToHost, stream);
+  return e == cudaSuccess ? PW_OK : cuda_fail(e, "planes to host");
+}
+
+int pw_planes_from_host(const void* host, uint32_t* planes, int32_t N, int32_t K, int32_t p_begin,
+                        cudaStream_t stream) {
+  size_t bytes = 0, off = 0;
+  int rc = pw::plane_tail_args(planes, host, N, K, p_begin, &bytes, &off);
+  if (rc) return rc;
+  if (bytes == 0) return PW_OK;
+  cudaError_t e = cudaMemcpyAsync(reinterpret_cast<char*>(planes) + off, host, bytes,
+                                  cudaMemcpyHostToDevice, stream);
+  return e == cudaSuccess ? PW_OK : cuda_fail(e, "planes from host");
 }
 
 int pw_page_table_read(const pw_page_table* t, pw_block_entry* host_out, cudaStream_t stream) {

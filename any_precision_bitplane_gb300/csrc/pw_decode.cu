@@ -723,19 +723,36 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
   int* count = psm;                 // [E]
   int* base = count + E;            // [E]
   int* wcnt = base + E;             // [kPrepWarps][E]
+  float* wsum = reinterpret_cast<float*>(wcnt + kPrepWarps * E);   // [E] routing mass
+  const bool stats = a.stats_counts != nullptr;
   __shared__ int s_warp_sum[kPrepWarps];
   __shared__ int s_bucket[2][8];
-  for (int e = tid; e < E; e += kPrepThreads) count[e] = 0;
+  for (int e = tid; e < E; e += kPrepThreads) {
+    count[e] = 0;
+    wsum[e] = 0.f;
+  }
   for (int i = tid; i < kPrepWarps * E; i += kPrepThreads) wcnt[i] = 0;
   if (tid < 16) (&s_bucket[0][0])[tid] = 0;
   for (int i = tid; i < (a.H + 31) / 32; i += kPrepThreads) w.arrive[i] = 0;
   __syncthreads();
   for (int p = tid; p < P; p += kPrepThreads) {
     const int e = a.topk_ids[p];
-    if (e >= 0 && e < E) atomicAdd(&count[e], 1);
-    else latch_status(a.status, PW_ERR_BAD_EXPERT_ID);
+    if (e >= 0 && e < E) {
+      atomicAdd(&count[e], 1);
+      if (stats) atomicAdd(&wsum[e], a.topk_weights[p]);
+    } else {
+      latch_status(a.status, PW_ERR_BAD_EXPERT_ID);
+    }
   }
   __syncthreads();
+  if (stats) {   // routing statistics, a by-product of the grouping
+    for (int e = tid; e < E; e += kPrepThreads) {
+      if (count[e] > 0) {
+        atomicAdd(&a.stats_counts[e], count[e]);
+        atomicAdd(&a.stats_mass[e], wsum[e]);
+      }
+    }
+  }
   // exclusive scan of count -> base / offsets
   const int per = (E + kPrepThreads - 1) / kPrepThreads;
   const int lo = min(E, tid * per), hi = min(E, lo + per);
@@ -940,7 +957,7 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
   const bool heavy = hybrid && hybrid_possible(shape);
   w.heavy_min = heavy ? kHeavyMinTokens : 0;
 
-  const size_t prep_smem = sizeof(int) * static_cast<size_t>(a.E) * (2 + kPrepWarps);
+  const size_t prep_smem = sizeof(int) * static_cast<size_t>(a.E) * (3 + kPrepWarps);
   if (prep_smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(decode_prep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -11,6 +11,8 @@ struct pw_page_table {
   int device;
   pw_block_entry* d_entries;  // fixed device address for the table's lifetime
   int32_t* d_status;          // first device-side error latched by forward calls
+  int32_t* stats_counts = nullptr;  // routing statistics (caller's buffers) or NULL
+  float* stats_mass = nullptr;
 };
 
 namespace pw {
@@ -73,7 +75,12 @@ struct LayerArgs {
   const pw_block_entry* table;   // [2E]
   float* out;                    // [T][H]
   int32_t* status;
+  int32_t* stats_counts;         // [E] routing statistics to accumulate, or NULL
+  float* stats_mass;             // [E]
 };
+// Routing statistics of one call (pairs per expert, sum of their weights),
+// added to a.stats_counts / a.stats_mass; no-op when they are NULL.
+cudaError_t launch_routing_stats(const LayerArgs& a, cudaStream_t s);
 // Experts with at least this many pairs in a decode call go through the
 // tensor-core GEMM kernels of the prefill path (when the shape allows it);
 // the others through the decode kernels.

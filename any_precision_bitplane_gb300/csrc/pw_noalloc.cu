@@ -106,6 +106,8 @@ extern "C" int pw_moe_forward_noalloc(const pw_moe_shape* shape, const void* hid
   a.table = table->d_entries;
   a.out = out;
   a.status = table->d_status;
+  a.stats_counts = table->stats_counts;
+  a.stats_mass = table->stats_mass;
   e = pw::launch_decode(a, scratch, stream, false);
   if (e != cudaSuccess) return pw::cuda_fail(e, "forward launch");
   return PW_OK;

@@ -1019,6 +1019,7 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   cudaError_t e = launch_permute(la.topk_ids, n_pairs, la.E, w.offsets, w.perm, nullptr, la.status,
                                  stream);
   if (e != cudaSuccess) return e;
+  if ((e = launch_routing_stats(la, stream)) != cudaSuccess) return e;
   const long long gwork = static_cast<long long>(n_pairs) * (la.H / 8);
   const int gblocks = static_cast<int>(std::min<long long>((gwork + 255) / 256, 152LL * 32));
   gather_kernel<<<gblocks, 256, 0, stream>>>(la.hidden, w.perm, w.offsets, la.E, la.k, la.H,

@@ -181,4 +181,31 @@ cudaError_t launch_permute(const int32_t* ids, int n_pairs, int E, int32_t* offs
   return cudaGetLastError();
 }
 
+namespace {
+
+__global__ void __launch_bounds__(256) routing_stats_kernel(const int32_t* __restrict__ ids,
+                                                            const float* __restrict__ wts,
+                                                            int n_pairs, int E,
+                                                            int32_t* __restrict__ counts,
+                                                            float* __restrict__ mass) {
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < n_pairs; p += gridDim.x * blockDim.x) {
+    const int e = ids[p];
+    if (e < 0 || e >= E) continue;
+    atomicAdd(&counts[e], 1);
+    atomicAdd(&mass[e], wts[p]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_routing_stats(const LayerArgs& a, cudaStream_t s) {
+  if (a.stats_counts == nullptr) return cudaSuccess;
+  const int n_pairs = a.T * a.k;
+  if (n_pairs == 0) return cudaSuccess;
+  const int blocks = (n_pairs + 255) / 256 < 1024 ? (n_pairs + 255) / 256 : 1024;
+  routing_stats_kernel<<<blocks, 256, 0, s>>>(a.topk_ids, a.topk_weights, n_pairs, a.E,
+                                              a.stats_counts, a.stats_mass);
+  return cudaGetLastError();
+}
+
 }  // namespace pw

@@ -199,6 +199,77 @@ int32_t pw_page_table_size(const pw_page_table* table);
 int pw_page_table_status(pw_page_table* table, int32_t* host_status, int32_t reset,
                          cudaStream_t stream);
 
+/* Online routing statistics (PagedWeight, "Core components" 2: the planner
+ * tracks each expert's routing mass, its selection frequency and weight).
+ * While set, every forward call through `table` adds, for each expert e,
+ *   counts[e] += number of (token, j) pairs routed to e,
+ *   mass[e]   += sum of their topk_weights,
+ * as a by-product of grouping the pairs (pairs with an id outside [0, E) are
+ * left out).  counts: device int32 [E]; mass: device float [E]; both owned and
+ * zeroed by the caller, who reads them back (e.g. to derive hot experts for the
+ * planner).  Pass NULL, NULL to stop.  The float sums are accumulated with
+ * atomics, so their last bits depend on the order of the additions.
+ * Errors: PW_ERR_INVALID_ARG (NULL table, exactly one buffer NULL). */
+int pw_page_table_set_routing_stats(pw_page_table* table, int32_t* counts, float* mass);
+
+/* ---- page movement ---------------------------------------------------------
+ * PagedWeight, "Core components" 3: weight pages are offloaded to CPU RAM and
+ * reloaded asynchronously to hide the latency; a bitwidth commit takes effect
+ * only at a safe boundary.  Planes are plane-major ([8][K/32][N]), so the tail
+ * planes p >= q of a block, which a forward call at bitwidth q never reads,
+ * are one contiguous run: lowering q frees them, raising q needs them back.
+ *
+ * Copy planes [p_begin, 8) of a block (device, N rows, K columns) to pinned
+ * host memory, or back, on `stream` (asynchronous; one cudaMemcpyAsync).
+ * host: (8 - p_begin) * N * K / 8 bytes.  Errors: PW_ERR_INVALID_ARG (NULL,
+ * unaligned planes, p_begin outside 0..7, N < 0), PW_ERR_SHAPE (K % 32),
+ * PW_ERR_CUDA. */
+int pw_planes_to_host(const uint32_t* planes, int32_t N, int32_t K, int32_t p_begin, void* host,
+                      cudaStream_t stream);
+int pw_planes_from_host(const void* host, uint32_t* planes, int32_t N, int32_t K, int32_t p_begin,
+                        cudaStream_t stream);
+
+/* pw_page_table_commit ordered after `ready` (e.g. an event recorded on the
+ * copy stream after pw_planes_from_host): `stream` waits for the event, then
+ * commits, so forward calls enqueued on `stream` before this call read the old
+ * bitwidths and calls after it the new ones, never a half-copied tail.
+ * Errors: as pw_page_table_commit, plus PW_ERR_CUDA. */
+int pw_page_table_commit_after(pw_page_table* table, int32_t n, const int32_t* block_ids,
+                               const int32_t* new_q, const uint16_t* const* new_lut,
+                               cudaEvent_t ready, cudaStream_t stream);
+
+/* ---- planner ----------------------------------------------------------------
+ * Greedy damage-per-byte planner (PagedWeight, "Core components" 2: when a
+ * memory target is set, the planner scores the damage of each possible
+ * bitwidth cut and greedily takes the cuts with the least damage per byte
+ * saved; frequently routed experts are protected by higher bitwidth floors
+ * and damage multipliers).  Host-only computation; its output is the list a
+ * pw_page_table_commit applies.
+ *   n_blocks       2E blocks, block 2e = gate_up and 2e+1 = down of expert e
+ *   q_now          host int32 [n_blocks], current bitwidths (3,4,5,6,8)
+ *   sensitivity    host float [n_blocks], damage per unit of quantisation error (>= 0)
+ *   bytes_per_bit  host int64 [n_blocks], bytes of one bitplane of the block (N*K/8)
+ *   routing_mass   host float [E], each expert's routing mass (>= 0), e.g. the
+ *                  mass accumulated by pw_page_table_set_routing_stats
+ *   hot_floor      bitwidth floor of hot experts (3,4,5,6,8); an expert is hot
+ *                  when its share of the total mass exceeds 1/E; others: floor 3
+ *   bytes_to_free  the memory target
+ * A cut lowers one block by one rung of 8 > 6 > 5 > 4 > 3, from b to b', and
+ *   damage = sensitivity * m_e * (4^-b' - 4^-b),  m_e = max(1, E * share_e),
+ *   bytes  = (b - b') * bytes_per_bit
+ * (4^-b: the relative error of a b-bit quantiser).  The planner repeatedly
+ * applies the cut with the least damage per byte (ties: lower block id) until
+ * at least bytes_to_free bytes are saved or no cut is left.
+ * Outputs: out_ids / out_q (host int32 [n_blocks]) = the blocks whose bitwidth
+ * changed, ascending id, and their new bitwidth; *n_out their number;
+ * *bytes_freed the bytes the cuts save.
+ * Errors: PW_ERR_INVALID_ARG (NULL pointer, n_blocks odd or negative, negative
+ * input), PW_ERR_UNSUPPORTED_Q (a bitwidth off the ladder). */
+int pw_plan_recommit(int32_t n_blocks, const int32_t* q_now, const float* sensitivity,
+                     const int64_t* bytes_per_bit, const float* routing_mass, int32_t hot_floor,
+                     int64_t bytes_to_free, int32_t* out_ids, int32_t* out_q, int32_t* n_out,
+                     int64_t* bytes_freed);
+
 /* ---- the fused layer ------------------------------------------------------
  * Bytes of device workspace a forward call of this shape needs. */
 int pw_workspace_bytes(const pw_moe_shape* shape, size_t* bytes);

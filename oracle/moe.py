@@ -66,6 +66,19 @@ def permute(topk_ids: np.ndarray, E: int):
     return offsets.astype(np.int32), perm.astype(np.int32), inv.astype(np.int32)
 
 
+def routing_stats(topk_ids: np.ndarray, topk_weights: np.ndarray, E: int):
+    """Online routing statistics (PagedWeight, "Core components" 2: an
+    expert's routing mass is how often it is selected and with what weight).
+    Per expert: the number of (token, j) pairs routed to it and the sum of
+    their weights (fp64).  Ids outside [0, E) are left out."""
+    ids = np.asarray(topk_ids).ravel()
+    w = np.asarray(topk_weights, dtype=np.float64).ravel()
+    valid = (ids >= 0) & (ids < E)
+    counts = np.bincount(ids[valid], minlength=E).astype(np.int64)
+    mass = np.bincount(ids[valid], weights=w[valid], minlength=E)
+    return counts, mass
+
+
 def silu(g: np.ndarray) -> np.ndarray:
     return g / (1.0 + np.exp(-g))
 

@@ -97,3 +97,35 @@ def test_forward_rejects_null_table(pw):
     s = pw.MoeShape(4, 256, 512, 8, 2)
     rc = L.pw_moe_forward(ctypes.byref(s), None, None, None, None, None, None, 0, None)
     assert rc == pw.PW_ERR_INVALID_ARG
+
+
+# The planner is a host computation inside libpw: it runs without a GPU.
+
+def test_planner_matches_oracle(pw):
+    import numpy as np
+    from oracle import planner
+    rng = np.random.default_rng(5)
+    for trial in range(30):
+        E = int(rng.integers(1, 40))
+        n = 2 * E
+        q_now = rng.choice(planner.LADDER, n).astype(np.int32)
+        sens = rng.lognormal(0, 1.5, n).astype(np.float32)
+        if trial % 3 == 0:
+            sens[:] = np.float32(1.0)          # many equal ratios: the tie-break decides
+        bpb = rng.integers(0, 1 << 20, n)
+        mass = rng.exponential(1.0, E).astype(np.float32)
+        target = int(rng.integers(0, int(bpb.sum()) * 3 + 1))
+        hot_floor = int(rng.choice(planner.LADDER))
+        want = planner.plan_recommit(q_now.tolist(), sens, bpb.tolist(), mass, hot_floor, target)
+        got = pw.plan_recommit(q_now, sens, bpb, mass, hot_floor, target)
+        assert got == want, trial
+
+
+def test_planner_rejects_bad_input(pw):
+    with pytest.raises(pw.PWError) as ei:
+        pw.plan_recommit([8, 7], [1, 1], [10, 10], [1.0], 6, 5)
+    assert ei.value.code == pw.PW_ERR_UNSUPPORTED_Q
+    with pytest.raises(pw.PWError) as ei:
+        pw.plan_recommit([8, 8, 8], [1, 1, 1], [10, 10, 10], [1.0], 6, 5)
+    assert ei.value.code == pw.PW_ERR_INVALID_ARG
+    assert pw.plan_recommit([], [], [], [], 6, 5) == ([], [], 0)

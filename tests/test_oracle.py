@@ -10,7 +10,7 @@ import os
 import numpy as np
 import pytest
 
-from oracle import apl, moe
+from oracle import apl, moe, planner
 from workloads import configs, gen
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -196,6 +196,33 @@ def test_permute_empty_and_out_of_range():
         moe.permute(np.array([[0, 4]], np.int32), 4)
 
 
+def test_routing_stats_brute_force_and_invariants():
+    # brute force: a plain loop over the pairs; invariants: every valid pair
+    # counted once, and the renormalised router weights of a token sum to 1,
+    # so the total routing mass equals the number of tokens
+    rng = np.random.default_rng(7)
+    T, E, k = 37, 9, 3
+    ids, w = moe.route_topk(rng.standard_normal((T, E)), k)
+    counts, mass = moe.routing_stats(ids, w, E)
+    c_ref, m_ref = [0] * E, [0.0] * E
+    for t in range(T):
+        for j in range(k):
+            c_ref[int(ids[t, j])] += 1
+            m_ref[int(ids[t, j])] += float(w[t, j])
+    assert counts.tolist() == c_ref
+    np.testing.assert_allclose(mass, m_ref, rtol=1e-12)
+    assert counts.sum() == T * k
+    assert math.isclose(mass.sum(), T, rel_tol=1e-12)
+
+
+def test_routing_stats_skips_out_of_range_ids():
+    ids = np.array([[0, 5], [-1, 2]], np.int32)
+    w = np.array([[0.25, 0.75], [0.5, 0.5]])
+    counts, mass = moe.routing_stats(ids, w, 4)
+    assert counts.tolist() == [1, 0, 1, 0]
+    assert mass.tolist() == [0.25, 0.0, 0.5, 0.0]
+
+
 # ---------------------------------------------------------------- SiLU
 
 def test_silu_textbook_values():
@@ -366,3 +393,59 @@ def test_recommit_lowers_one_rung_above_floor():
     ladder = [3, 4, 5, 6, 8]
     for o, n, f in zip(old, new_q, floor[ids]):
         assert ladder.index(int(n)) == ladder.index(int(o)) - 1 and n >= f
+
+
+# ---------------------------------------------------------------- planner
+
+def _planner_example():
+    return dict(q_now=[8, 6, 8, 4], sensitivity=[1.5, 1, 2, 1], bytes_per_bit=[100] * 4,
+                routing_mass=[3, 1], hot_floor=6)
+
+
+def test_planner_worked_example():
+    for target, ids, qs, freed in _read_golden("planner_worked_example.txt"):
+        got = planner.plan_recommit(bytes_to_free=int(target), **_planner_example())
+        want_ids = [] if ids == "-" else [int(x) for x in ids.split(",")]
+        want_q = [] if qs == "-" else [int(x) for x in qs.split(",")]
+        assert got == (want_ids, want_q, int(freed)), target
+
+
+def test_planner_equal_blocks_cut_least_sensitive_first():
+    # equal sizes, no hot expert, sensitivities within a factor 6 of each
+    # other: every first cut (8 -> 6) is cheaper per byte than any second one,
+    # so the first m cuts are the m least sensitive blocks (a stable argsort)
+    rng = np.random.default_rng(3)
+    n, m = 24, 7
+    sens = rng.uniform(1.0, 5.0, n).astype(np.float32)
+    ids, qs, freed = planner.plan_recommit([8] * n, sens, [64] * n, [1.0] * (n // 2), 6,
+                                           m * 2 * 64)
+    assert ids == sorted(np.argsort(sens, kind="stable")[:m].tolist())
+    assert qs == [6] * m and freed == m * 2 * 64
+
+
+def test_planner_invariants_random():
+    rng = np.random.default_rng(11)
+    for trial in range(20):
+        E = int(rng.integers(1, 12))
+        n = 2 * E
+        q_now = rng.choice(planner.LADDER, n).tolist()
+        sens = rng.lognormal(0, 1, n).astype(np.float32)
+        bpb = rng.integers(0, 5000, n).tolist()
+        mass = rng.exponential(1.0, E).astype(np.float32)
+        target = int(rng.integers(0, 60000))
+        trace = []
+        ids, qs, freed = planner.plan_recommit(q_now, sens, bpb, mass, 6, target, trace)
+        total = float(sum(float(m) for m in mass))
+        new = list(q_now)
+        for i, q in zip(ids, qs):
+            new[i] = q
+        for i in range(n):
+            assert new[i] <= q_now[i]                                   # only lowered
+            hot = float(mass[i // 2]) * E > total
+            if new[i] != q_now[i]:
+                assert new[i] >= (6 if hot else 3)                      # floors respected
+        assert freed == sum((q_now[i] - new[i]) * bpb[i] for i in range(n))
+        ratios = [r for r, _, _ in trace]
+        assert ratios == sorted(ratios)                                 # greedy order
+        if freed < target:                                              # nothing left to cut
+            assert planner.plan_recommit(new, sens, bpb, mass, 6, 1)[2] == 0

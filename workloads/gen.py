@@ -145,3 +145,11 @@ def make_recommit(layer: Layer, seed: int = 1) -> Tuple[np.ndarray, np.ndarray]:
     ladder = list(BITWIDTHS)
     new_q = np.array([ladder[ladder.index(int(q[b])) - 1] for b in chosen], dtype=np.int32)
     return chosen, new_q
+
+
+def make_sensitivity(layer: Layer, seed: int = 2) -> np.ndarray:
+    """Synthetic offline sensitivity per block [2E] (block 2e gate_up, 2e+1
+    down): log-normal(0, 1) damage scores standing in for the Hessian-weighted
+    scores the planner reads (no trained weights are used)."""
+    rng = np.random.default_rng(seed)
+    return rng.lognormal(0.0, 1.0, 2 * layer.cfg.E).astype(np.float32)
