@@ -258,41 +258,60 @@ def time_dominant(pw, cfg, layers, hidden, ids, wts, steps, stream):
 
 
 def time_e2e(pw, cfg, layers, host, steps, warmup, device):
-    """Through the public API with host buffers: per step, H2D of the step's
-    inputs from pinned memory, the forward call, D2H of the output."""
+    """End to end through the C ABI with HOST buffers: every step hands
+    pw_moe_forward pinned host pointers for hidden, topk ids, topk weights and
+    out, so the step's inputs travel host -> device and its result device ->
+    host inside the call (the kernels read and write the pinned pages directly
+    over the CPU-GPU link; the pointers are valid on the device under unified
+    addressing).  The K steps are captured in one CUDA graph and timed on the
+    wall clock around its replay; the last output is checked against the same
+    call on device buffers."""
+    import ctypes
     import torch
     T = host["hidden"].shape[0]
-    h_hidden = torch.from_numpy(host["hidden"]).pin_memory()
-    h_ids = torch.from_numpy(host["ids"]).pin_memory()
-    h_wts = torch.from_numpy(host["wts"]).pin_memory()
-    h_out = torch.empty((T, cfg.H), dtype=torch.float32).pin_memory()
-    d_hidden = torch.empty_like(h_hidden, device=device)
-    d_ids = torch.empty_like(h_ids, device=device)
-    d_wts = torch.empty_like(h_wts, device=device)
-    d_out = torch.empty((T, cfg.H), dtype=torch.float32, device=device)
-    ws = torch.empty(max(pw.workspace_bytes(T, cfg.H, cfg.I, cfg.E, cfg.k), 256),
-                     dtype=torch.uint8, device=device)
+    k = host["ids"].shape[1]
+    h_hidden = torch.from_numpy(host["hidden"].copy()).pin_memory()
+    h_ids = torch.from_numpy(host["ids"].astype(np.int32)).pin_memory()
+    h_wts = torch.from_numpy(host["wts"].astype(np.float32)).pin_memory()
+    h_out = torch.zeros((T, cfg.H), dtype=torch.float32).pin_memory()
+    ws_bytes = max(pw.workspace_bytes(T, cfg.H, cfg.I, cfg.E, cfg.k), 256)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    shape = pw.MoeShape(T, cfg.H, cfg.I, cfg.E, k)
     L = len(layers)
+    stream = torch.cuda.Stream(device)
+    lib = pw.lib()
 
     def step(i):
-        d_hidden.copy_(h_hidden, non_blocking=True)
-        d_ids.copy_(h_ids, non_blocking=True)
-        d_wts.copy_(h_wts, non_blocking=True)
-        pw.moe_forward(d_hidden, d_ids, d_wts, layers[i % L].table, cfg.I, cfg.E, out=d_out,
-                       workspace=ws)
-        h_out.copy_(d_out, non_blocking=True)
+        rc = lib.pw_moe_forward(ctypes.byref(shape), ctypes.c_void_p(h_hidden.data_ptr()),
+                                ctypes.c_void_p(h_ids.data_ptr()),
+                                ctypes.c_void_p(h_wts.data_ptr()), layers[i % L].table.handle,
+                                ctypes.c_void_p(h_out.data_ptr()),
+                                ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws_bytes),
+                                ctypes.c_void_p(stream.cuda_stream))
+        if rc != pw.PW_OK:
+            raise RuntimeError("pw_moe_forward (host buffers): %s" % pw.last_error())
 
-    for i in range(warmup):
-        step(i)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(steps):
-        step(i)
-    torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps):
+                step(i)
+        g.replay()                     # instantiation/upload, untimed
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        g.replay()
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+    ref = pw.moe_forward(h_hidden.to(device), h_ids.to(device), h_wts.to(device),
+                         layers[(steps - 1) % L].table, cfg.I, cfg.E)
+    if not torch.equal(ref.cpu(), h_out):
+        raise RuntimeError("e2e: the host-buffer output differs from the device-buffer call")
+    del g
     bi = h_hidden.numel() * 2 + h_ids.numel() * 4 + h_wts.numel() * 4
-    bo = h_out.numel() * 4
-    return dt, bi, bo
+    return dt, bi, h_out.numel() * 4
 
 
 def _oracle_setup(name, T):
@@ -492,7 +511,9 @@ def native(args):
     if not args.no_e2e:
         e2e_dt, bi, bo = time_e2e(pw, cfg, layers, host, args.steps, args.warmup, device)
         e2e = {"value": T * args.steps * world / e2e_dt, "unit": "tokens/s",
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "mode": "C ABI with pinned host buffers read/written by the kernels, K steps "
+                       "in one CUDA graph, wall clock"}
 
     sweep = {}
     if not args.no_sweep and rank == 0 and world == 1:

@@ -287,6 +287,11 @@ int pw_workspace_bytes(const pw_moe_shape* shape, size_t* bytes);
  *   out          device float [T][H] (output, overwritten)
  *   workspace    device scratch of >= pw_workspace_bytes(shape) bytes, 256-byte
  *                aligned; it must not be in use by another call in flight
+ * hidden, topk_ids, topk_weights and out may also be pinned host memory that
+ * the device addresses with the same pointer (cudaHostAlloc or
+ * cudaHostRegister under unified addressing): the kernels then read the
+ * inputs and write the output across the CPU-GPU link themselves, so a step
+ * needs no separate copies.
  * The call allocates nothing and never synchronises the host; it can be
  * captured in a CUDA graph.  Errors: PW_ERR_INVALID_ARG, PW_ERR_SHAPE,
  * PW_ERR_WORKSPACE, PW_ERR_UNSUPPORTED_DEVICE, PW_ERR_CUDA. */
