@@ -185,40 +185,52 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// LUT rows of one pass into shared memory as fp32 (layouts above).  Each
-// thread moves up to four 16-byte pieces (8 fp16 entries each); all of its
-// loads are issued before the first store, so a pass waits for one memory
-// round trip.  A warp's stores hit 32 banks.
-template <int Q, int R, bool COMPACT>
-__device__ __forceinline__ void load_luts(const uint16_t* lut, const PassRows<R>& pr,
-                                          const SmemPtrs& s) {
-  constexpr int kEnt = 1 << Q;
-  constexpr int kVecPerRow = kEnt / 8;
-  constexpr int kPerSlot = 32 * kVecPerRow;
-  constexpr int kTotal = R * kPerSlot;
-  constexpr int kPer = (kTotal + kThreads - 1) / kThreads;
+// LUT rows of one pass into shared memory as fp32 (layouts above), in two
+// steps so that the round trip overlaps other set-up work: lut_fetch issues
+// every global load of the thread (up to four 16-byte pieces of 8 fp16
+// entries) into registers, lut_store converts and stores them.  A warp's
+// stores hit 32 banks.
+template <int Q, int R>
+struct LutPieces {
+  static constexpr int kEnt = 1 << Q;
+  static constexpr int kVecPerRow = kEnt / 8;
+  static constexpr int kPerSlot = 32 * kVecPerRow;
+  static constexpr int kTotal = R * kPerSlot;
+  static constexpr int kPer = (kTotal + kThreads - 1) / kThreads;
   uint4 raw[kPer];
+};
+
+template <int Q, int R>
+__device__ __forceinline__ void lut_fetch(const uint16_t* lut, const PassRows<R>& pr,
+                                          LutPieces<Q, R>& lp) {
+  using L = LutPieces<Q, R>;
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
+  for (int j = 0; j < L::kPer; ++j) {
     const int i = threadIdx.x + j * kThreads;
-    if (i < kTotal) {
-      const int g = i / kPerSlot, rem = i % kPerSlot;
-      const int L = rem & 31, vec = rem >> 5;
-      const int row = seg_base<R>(pr, g, L >> 4) + (L & 15);
-      raw[j] = __ldg(reinterpret_cast<const uint4*>(lut + static_cast<long long>(row) * kEnt + vec * 8));
+    if (i < L::kTotal) {
+      const int g = i / L::kPerSlot, rem = i % L::kPerSlot;
+      const int lane = rem & 31, vec = rem >> 5;
+      const int row = seg_base<R>(pr, g, lane >> 4) + (lane & 15);
+      lp.raw[j] = __ldg(reinterpret_cast<const uint4*>(lut + static_cast<long long>(row) * L::kEnt +
+                                                       vec * 8));
     }
   }
+}
+
+template <int Q, int R, bool COMPACT>
+__device__ __forceinline__ void lut_store(const LutPieces<Q, R>& lp) {
+  using L = LutPieces<Q, R>;
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
+  for (int j = 0; j < L::kPer; ++j) {
     const int i = threadIdx.x + j * kThreads;
-    if (i < kTotal) {
-      const int g = i / kPerSlot, rem = i % kPerSlot;
-      const int L = rem & 31, vec = rem >> 5;
-      const __half* h = reinterpret_cast<const __half*>(&raw[j]);
+    if (i < L::kTotal) {
+      const int g = i / L::kPerSlot, rem = i % L::kPerSlot;
+      const int lane = rem & 31, vec = rem >> 5;
+      const __half* h = reinterpret_cast<const __half*>(&lp.raw[j]);
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const int v = vec * 8 + jj;
-        const int off = COMPACT ? v * 128 + L * 4 : v * 256 + g * 128 + L * 4;
+        const int off = COMPACT ? v * 128 + lane * 4 : v * 256 + g * 128 + lane * 4;
         *reinterpret_cast<float*>(g_dsmem + off) = __half2float(h[jj]);
       }
     }
@@ -376,17 +388,6 @@ __device__ __forceinline__ void warp_range(int KW, int& lo, int& hi) {
 }
 
 
-// Tile ids: a CTA's first tile is its block index; later ones come from a
-// global counter (offset by the grid size) and are broadcast to the CTA.
-__device__ __forceinline__ int next_tile(int* counter, int* slot, bool first) {
-  if (first) return blockIdx.x;
-  if (threadIdx.x == 0) *slot = gridDim.x + atomicAdd(counter, 1);
-  __syncthreads();
-  const int t = *slot;
-  __syncthreads();
-  return t;
-}
-
 // ---------------------------------------------------------------- gate_up
 
 // One token group of one pass.  Paired passes (R = 2): slot 0 = gate rows
@@ -416,7 +417,8 @@ __device__ void gateup_prime(const LayerArgs& a, const DecodeWs& w, const Expert
 template <int Q, int R, bool COMPACT, int NT>
 __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
                              const SlotInfo& ent, const PassRows<R>& pr, int hcol0, int g0,
-                             int nt, const SmemPtrs& s, const BitConsts& bc, bool primed) {
+                             int nt, const SmemPtrs& s, const BitConsts& bc, bool primed,
+                             int* claim_counter) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int KW = a.H / 32;
   const long long N = 2LL * a.I;
@@ -426,6 +428,10 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
   gateup_xs<NT>(a, w, ex, g0, nt, xs);
   float2 acc[R][NT];
   rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc, primed);
+  // the tile's last group claims the CTA's next tile; the atomic's round
+  // trip overlaps the reduction and the epilogue
+  int claim = 0;
+  if (claim_counter && threadIdx.x == 0) claim = atomicAdd(claim_counter, 1);
 #pragma unroll
   for (int tk = 0; tk < NT; ++tk)
 #pragma unroll
@@ -447,34 +453,40 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
       w.h[static_cast<long long>(ex.off + g0 + tk) * a.I + hcol0 + lane] = h;
     }
   }
+  if (claim_counter && threadIdx.x == 0) s.misc[2] = claim;
   __syncthreads();
 }
 
 template <int Q, int R, bool COMPACT>
 __device__ void gateup_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
                             const SlotInfo& ent, const PassRows<R>& pr, int hcol0,
-                            const SmemPtrs& s, const BitConsts& bc) {
+                            const SmemPtrs& s, const BitConsts& bc, int* claim_counter) {
   __syncthreads();  // the previous pass is done with the LUT region and the rings
-  // the first token group's first columns start loading before the LUT does
+  // the LUT loads go out first, then the first token group's first columns
+  // (whose activation rows need one more dependent load), so that both
+  // round trips overlap
+  LutPieces<Q, R> lp;
+  lut_fetch<Q, R>(ent.lut, pr, lp);
   const int nt0 = min(kTG, ex.ne);
   if (nt0 == 1) gateup_prime<Q, R, 1>(a, w, ex, ent, pr, 0, nt0);
   else if (nt0 == 2) gateup_prime<Q, R, 2>(a, w, ex, ent, pr, 0, nt0);
   else gateup_prime<Q, R, 4>(a, w, ex, ent, pr, 0, nt0);
-  load_luts<Q, R, COMPACT>(ent.lut, pr, s);
+  lut_store<Q, R, COMPACT>(lp);
   __syncthreads();
   for (int g0 = 0; g0 < ex.ne; g0 += kTG) {
     const int nt = min(kTG, ex.ne - g0);
     const bool primed = (g0 == 0);
-    if (nt == 1) gateup_group<Q, R, COMPACT, 1>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed);
-    else if (nt == 2) gateup_group<Q, R, COMPACT, 2>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed);
-    else gateup_group<Q, R, COMPACT, 4>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed);
+    int* cc = (g0 + kTG >= ex.ne) ? claim_counter : nullptr;
+    if (nt == 1) gateup_group<Q, R, COMPACT, 1>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed, cc);
+    else if (nt == 2) gateup_group<Q, R, COMPACT, 2>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed, cc);
+    else gateup_group<Q, R, COMPACT, 4>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed, cc);
   }
 }
 
 template <int Q>
 __device__ void gateup_tile(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
                             const SlotInfo& ent, int i0, const SmemPtrs& s,
-                            const BitConsts& bc) {
+                            const BitConsts& bc, int* claim_counter) {
   if (Q == 8) {
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
@@ -482,7 +494,7 @@ __device__ void gateup_tile(const LayerArgs& a, const DecodeWs& w, const ExpertW
       PassRows<1> pr;
       pr.seg[0][0] = i;
       pr.seg[0][1] = a.I + i;
-      gateup_pass<8, 1, true>(a, w, ex, ent, pr, i, s, bc);
+      gateup_pass<8, 1, true>(a, w, ex, ent, pr, i, s, bc, half ? claim_counter : nullptr);
     }
   } else {
     PassRows<2> pr;
@@ -490,7 +502,7 @@ __device__ void gateup_tile(const LayerArgs& a, const DecodeWs& w, const ExpertW
     pr.seg[0][1] = i0 + 16;
     pr.seg[1][0] = a.I + i0;
     pr.seg[1][1] = a.I + i0 + 16;
-    gateup_pass<Q, 2, false>(a, w, ex, ent, pr, i0, s, bc);
+    gateup_pass<Q, 2, false>(a, w, ex, ent, pr, i0, s, bc, claim_counter);
   }
 }
 
@@ -502,23 +514,32 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerA
   allow_dependent_launch();    // the down kernel may start loading as CTAs retire
   const int tpe = a.I / kPairsPerTile;
   const int total = w.ctl[0] * tpe;
-  for (bool first = true;; first = false) {
-    const int t = next_tile(&w.ctl[1], &s.misc[0], first);
-    if (t >= total) break;
+  int* const counter = &w.ctl[1];
+  // A CTA's first tile is its block index; each tile claims the next one
+  // from the counter (offset by the grid size) and leaves it in misc[2].
+  for (int t = blockIdx.x; t < total;) {
     const int slot = t / tpe, x = t - slot * tpe;
     const SlotInfo si = w.routed_gu[slot];
-    if (si.err) {
-      if (x == 0 && threadIdx.x == 0) latch_status(a.status, si.err);
-      continue;
+    if (si.err || si.ne <= 0) {   // (a routed expert always holds a pair)
+      if (threadIdx.x == 0) {
+        if (si.err && x == 0) latch_status(a.status, si.err);
+        s.misc[2] = atomicAdd(counter, 1);
+      }
+      __syncthreads();
+    } else {
+      const ExpertWork ex{si.e, si.off, si.ne};
+      switch (si.q) {
+        case 3: gateup_tile<3>(a, w, ex, si, x * kPairsPerTile, s, bc, counter); break;
+        case 4: gateup_tile<4>(a, w, ex, si, x * kPairsPerTile, s, bc, counter); break;
+        case 5: gateup_tile<5>(a, w, ex, si, x * kPairsPerTile, s, bc, counter); break;
+        case 6: gateup_tile<6>(a, w, ex, si, x * kPairsPerTile, s, bc, counter); break;
+        default: gateup_tile<8>(a, w, ex, si, x * kPairsPerTile, s, bc, counter); break;
+      }
     }
-    const ExpertWork ex{si.e, si.off, si.ne};
-    switch (si.q) {
-      case 3: gateup_tile<3>(a, w, ex, si, x * kPairsPerTile, s, bc); break;
-      case 4: gateup_tile<4>(a, w, ex, si, x * kPairsPerTile, s, bc); break;
-      case 5: gateup_tile<5>(a, w, ex, si, x * kPairsPerTile, s, bc); break;
-      case 6: gateup_tile<6>(a, w, ex, si, x * kPairsPerTile, s, bc); break;
-      default: gateup_tile<8>(a, w, ex, si, x * kPairsPerTile, s, bc); break;
-    }
+    // claims only grow, so a tile id that does not advance ends the loop
+    const int next = static_cast<int>(gridDim.x) + s.misc[2];
+    t = next > t ? next : total;
+    __syncthreads();   // every thread has read the claim before it is overwritten
   }
 }
 
@@ -558,19 +579,24 @@ __device__ void down_group(const LayerArgs& a, const DecodeWs& w, const ExpertWo
   down_xs<NT>(a, w, ex, g0, nt, xs);
   float2 acc[R][NT];
   rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc, primed);
+  // thread i < 32*R*nt (at most kThreads) writes row slot (i/32)%R of token
+  // (i/32)/R; its pair id is loaded before the partial sums meet
+  const int i = threadIdx.x;
+  const bool writer = i < 32 * R * nt;
+  const int pair = writer ? w.perm[ex.off + g0 + (i >> 5) / R] : 0;
 #pragma unroll
   for (int tk = 0; tk < NT; ++tk)
 #pragma unroll
     for (int g = 0; g < R; ++g)
       s.red[((warp * kTG + tk) * 2 + g) * 32 + lane] = acc[g][tk].x + acc[g][tk].y;
   __syncthreads();
-  for (int i = threadIdx.x; i < 32 * R * nt; i += kThreads) {
-    const int L = i & 31, g = (i >> 5) % R, tk = (i >> 5) / R;
+  if (writer) {
+    const int g = (i >> 5) % R, tk = (i >> 5) / R;
     float y = 0.f;
 #pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) y += s.red[((ww * kTG + tk) * 2 + g) * 32 + L];
-    const int row = seg_base<R>(pr, g, L >> 4) + (L & 15);
-    w.y[static_cast<long long>(w.perm[ex.off + g0 + tk]) * a.H + row] = y;
+    for (int ww = 0; ww < kWarps; ++ww) y += s.red[((ww * kTG + tk) * 2 + g) * 32 + lane];
+    const int row = seg_base<R>(pr, g, lane >> 4) + (lane & 15);
+    w.y[static_cast<long long>(pair) * a.H + row] = y;
   }
   __syncthreads();
 }
@@ -580,7 +606,11 @@ __device__ void down_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWor
                           const SlotInfo& ent, const PassRows<R>& pr, const SmemPtrs& s,
                           const BitConsts& bc) {
   __syncthreads();
-  load_luts<Q, R, COMPACT>(ent.lut, pr, s);
+  {  // the LUT does not depend on h
+    LutPieces<Q, R> lp;
+    lut_fetch<Q, R>(ent.lut, pr, lp);
+    lut_store<Q, R, COMPACT>(lp);
+  }
   grid_dependency_wait();   // h is complete from here on
   const int nt0 = min(kTG, ex.ne);
   if (nt0 == 1) down_prime<Q, R, 1>(a, w, ex, ent, pr, 0, nt0);
@@ -648,9 +678,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArg
   }
   const int tpe = (a.H + kDownRows - 1) / kDownRows;
   const int total = n_routed * tpe;
-  for (bool first = true;; first = false) {
-    const int t = next_tile(&w.ctl[2], &s.misc[0], first);
-    if (t >= total) break;
+  // A CTA's first tile is its block index; each tile claims the next one
+  // from the counter (offset by the grid size) together with its arrival.
+  for (int t = blockIdx.x; t < total;) {
     const int slot = t / tpe, x = t - slot * tpe;
     const SlotInfo si = w.routed_dn[slot];
     const ExpertWork ex{si.e, si.off, si.ne};
@@ -671,9 +701,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArg
       }
     }
     // Arrival: the last routed expert to finish this row range combines it.
-    __threadfence();
+    // The barrier orders every thread's y stores before thread 0's fence and
+    // arrival (the release); the claim of the next tile shares the round trip.
     __syncthreads();
-    if (threadIdx.x == 0) s.misc[1] = (atomicAdd(&w.arrive[x], 1) == n_routed - 1);
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const int arrived = atomicAdd(&w.arrive[x], 1);
+      const int claim = atomicAdd(&w.ctl[2], 1);
+      s.misc[1] = (arrived == n_routed - 1);
+      s.misc[2] = claim;
+    }
     __syncthreads();
     if (s.misc[1]) {
       __threadfence();
@@ -689,6 +726,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArg
         a.out[static_cast<long long>(tt) * a.H + n] = acc;
       }
     }
+    const int next = static_cast<int>(gridDim.x) + s.misc[2];
+    t = next > t ? next : total;
+    __syncthreads();   // every thread has read the flags before they are overwritten
   }
 }
 
