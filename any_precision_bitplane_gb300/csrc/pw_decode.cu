@@ -21,8 +21,14 @@
 //            up rows I+i, rebuild the q-bit codes, look them up in each row's
 //            LUT, dot with the expert's tokens (fp32), h = SiLU(g) * u.
 //   down:    persistent CTAs take tiles (routed expert, 64 down rows): same
-//            read of the down block, dot with h -> y for each pair.  The last
-//            tile to finish a 64-row range (arrival counter) forms
+//            read of the down block, dot with h -> y for each pair.  When
+//            the down tiles are short (K = I <= kEarlyDownMaxI) a down tile
+//            waits only for its own expert's gate_up tiles (a per-expert
+//            counter that each finished gate_up tile increments after a
+//            fence), so down tiles fill the SMs that the gate_up tail leaves
+//            idle; long down tiles would slow the last gate_up tiles they
+//            share an SM with, so they wait for the whole gate_up grid.  The
+//            last tile to finish a 64-row range (arrival counter) forms
 //            out[t] = sum_j w_tj * y[t*k + j] over the range in j order, so
 //            the output is deterministic.
 //
@@ -125,6 +131,7 @@ struct DecodeWs {
   SlotInfo* routed_dn;  // [E] routed experts, down bitwidth descending
   int* ctl;        // [0] routed expert count, [1] gate_up tile counter, [2] down tile counter
   int* arrive;     // [H/32]   per 64-row range: down tiles finished
+  int* gu_done;    // [E]      gate_up tiles finished per expert (released by a fence)
   int heavy_min;   // experts with at least this many pairs are left to the GEMM kernels (0: none)
 };
 
@@ -388,6 +395,37 @@ __device__ __forceinline__ void warp_range(int KW, int& lo, int& hi) {
 }
 
 
+// Spin bound of the down kernel's wait for an expert's gate_up tiles; the
+// wait backs off with a short sleep, so the bound is well over a second.
+constexpr uint32_t kReadySpinLimit = 1u << 23;
+
+// Largest down-block K (= I) whose tiles start per expert (see above).
+constexpr int kEarlyDownMaxI = 8192;
+
+__device__ __forceinline__ int load_relaxed(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Thread 0 of a down CTA: wait until `need` gate_up tiles of the expert have
+// released their h rows.  `seen` is a poll issued earlier (relaxed, so that
+// it overlaps other loads); the closing fence makes the wait an acquire.
+// Gives up after kReadySpinLimit polls and latches PW_ERR_TIMEOUT (the tile
+// then runs on whatever h holds).
+__device__ __forceinline__ void wait_gate_up(const int* done, int seen, int need,
+                                             int32_t* status) {
+  for (uint32_t i = 0; seen < need; ++i) {
+    if (i == kReadySpinLimit) {
+      latch_status(status, PW_ERR_TIMEOUT);
+      break;
+    }
+    __nanosleep(128);
+    seen = load_relaxed(done);
+  }
+  __threadfence();
+}
+
 // ---------------------------------------------------------------- gate_up
 
 // One token group of one pass.  Paired passes (R = 2): slot 0 = gate rows
@@ -515,11 +553,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerA
   const int tpe = a.I / kPairsPerTile;
   const int total = w.ctl[0] * tpe;
   int* const counter = &w.ctl[1];
+  // Thread 0 releases a finished tile's h rows to the down kernel one tile
+  // late: by the next tile's descriptor load the stores have long landed,
+  // so the fence costs little.  The barriers since the tile's last h store
+  // order every thread's stores before thread 0's fence.
+  int pending = -1;
   // A CTA's first tile is its block index; each tile claims the next one
   // from the counter (offset by the grid size) and leaves it in misc[2].
   for (int t = blockIdx.x; t < total;) {
     const int slot = t / tpe, x = t - slot * tpe;
     const SlotInfo si = w.routed_gu[slot];
+    if (threadIdx.x == 0 && pending >= 0) {
+      __threadfence();
+      atomicAdd(&w.gu_done[pending], 1);
+      pending = -1;
+    }
     if (si.err || si.ne <= 0) {   // (a routed expert always holds a pair)
       if (threadIdx.x == 0) {
         if (si.err && x == 0) latch_status(a.status, si.err);
@@ -535,11 +583,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerA
         case 6: gateup_tile<6>(a, w, ex, si, x * kPairsPerTile, s, bc, counter); break;
         default: gateup_tile<8>(a, w, ex, si, x * kPairsPerTile, s, bc, counter); break;
       }
+      if (a.I <= kEarlyDownMaxI) pending = si.e;   // the down tiles wait per expert
     }
     // claims only grow, so a tile id that does not advance ends the loop
     const int next = static_cast<int>(gridDim.x) + s.misc[2];
     t = next > t ? next : total;
     __syncthreads();   // every thread has read the claim before it is overwritten
+  }
+  if (threadIdx.x == 0 && pending >= 0) {
+    __threadfence();
+    atomicAdd(&w.gu_done[pending], 1);
   }
 }
 
@@ -606,17 +659,23 @@ __device__ void down_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWor
                           const SlotInfo& ent, const PassRows<R>& pr, const SmemPtrs& s,
                           const BitConsts& bc) {
   __syncthreads();
+  // the expert's h rows are complete once all of its gate_up tiles released
+  // them: thread 0 polls (the first poll overlaps the LUT load) and acquires,
+  // and the barrier extends that to the CTA
+  const bool early = a.I <= kEarlyDownMaxI;
+  const int seen = (early && threadIdx.x == 0) ? load_relaxed(w.gu_done + ex.e) : 0;
   {  // the LUT does not depend on h
     LutPieces<Q, R> lp;
     lut_fetch<Q, R>(ent.lut, pr, lp);
     lut_store<Q, R, COMPACT>(lp);
   }
-  grid_dependency_wait();   // h is complete from here on
+  if (!early) grid_dependency_wait();   // the whole gate_up grid is done
+  else if (threadIdx.x == 0) wait_gate_up(w.gu_done + ex.e, seen, a.I / kPairsPerTile, a.status);
+  __syncthreads();
   const int nt0 = min(kTG, ex.ne);
   if (nt0 == 1) down_prime<Q, R, 1>(a, w, ex, ent, pr, 0, nt0);
   else if (nt0 == 2) down_prime<Q, R, 2>(a, w, ex, ent, pr, 0, nt0);
   else down_prime<Q, R, 4>(a, w, ex, ent, pr, 0, nt0);
-  __syncthreads();
   for (int g0 = 0; g0 < ex.ne; g0 += kTG) {
     const int nt = min(kTG, ex.ne - g0);
     const bool primed = (g0 == 0);
@@ -770,6 +829,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
   for (int e = tid; e < E; e += kPrepThreads) {
     count[e] = 0;
     wsum[e] = 0.f;
+    w.gu_done[e] = 0;
   }
   for (int i = tid; i < kPrepWarps * E; i += kPrepThreads) wcnt[i] = 0;
   if (tid < 16) (&s_bucket[0][0])[tid] = 0;
@@ -906,7 +966,7 @@ namespace {
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsSizes {
-  size_t x32, h, y, offsets, perm, routed, ctl, arrive;
+  size_t x32, h, y, offsets, perm, routed, ctl, arrive, gu_done;
 };
 
 WsSizes ws_sizes(const pw_moe_shape& s) {
@@ -920,6 +980,7 @@ WsSizes ws_sizes(const pw_moe_shape& s) {
   z.routed = round256(sizeof(SlotInfo) * static_cast<size_t>(s.E));
   z.ctl = 256;
   z.arrive = round256(4 * static_cast<size_t>(s.H / 32));
+  z.gu_done = round256(4 * static_cast<size_t>(s.E));
   return z;
 }
 
@@ -960,10 +1021,12 @@ bool hybrid_possible(const pw_moe_shape& s) {
 
 // Workspace: x32 [T][H] | h [T*k][I] | y [T*k][H] fp32 | offsets [E+1] |
 // perm [T*k] | routed lists [E] x 2 | control words | arrival counters [H/32]
-// | (when some expert can hold kHeavyMinTokens pairs) the GEMM kernels' scratch.
+// | gate_up tiles done [E] | (when some expert can hold kHeavyMinTokens pairs)
+// the GEMM kernels' scratch.
 size_t decode_workspace_bytes(const pw_moe_shape& s, bool hybrid) {
   const WsSizes z = ws_sizes(s);
-  const size_t base = z.x32 + z.h + z.y + z.offsets + z.perm + 2 * z.routed + z.ctl + z.arrive;
+  const size_t base =
+      z.x32 + z.h + z.y + z.offsets + z.perm + 2 * z.routed + z.ctl + z.arrive + z.gu_done;
   return base + ((hybrid && hybrid_possible(s)) ? heavy_scratch_bytes(s) : 0);
 }
 
@@ -994,6 +1057,7 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
   w.routed_dn = reinterpret_cast<SlotInfo*>(p); p += z.routed;
   w.ctl = reinterpret_cast<int*>(p); p += z.ctl;
   w.arrive = reinterpret_cast<int*>(p); p += z.arrive;
+  w.gu_done = reinterpret_cast<int*>(p); p += z.gu_done;
   const bool heavy = hybrid && hybrid_possible(shape);
   w.heavy_min = heavy ? kHeavyMinTokens : 0;
 

@@ -332,7 +332,7 @@ int pw_set_timing_events(cudaEvent_t before, cudaEvent_t after);
  * workspace: the scratch lives in one static device array of 8 MiB inside
  * libpw (every GPU that loads the library keeps those 8 MiB until the process
  * exits).  The caller still passes inputs and outputs.
- *   - Shapes whose decode scratch, about 4*T*H + 4*T*k*(I + H + 1) + 84*E
+ *   - Shapes whose decode scratch, about 4*T*H + 4*T*k*(I + H + 1) + 88*E
  *     + H/8 bytes (each section rounded up to 256 bytes), exceeds 8 MiB are
  *     rejected with
  *     PW_ERR_WORKSPACE (use pw_moe_forward with a workspace instead), as
