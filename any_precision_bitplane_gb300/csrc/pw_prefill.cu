@@ -37,11 +37,15 @@
 //   warp 22     allocates the 512 TMEM columns; lane 0 issues per k-step two
 //               K=16 steps of two tcgen05.mma (M=128, N=256 each, fp16 x
 //               fp16 -> fp32) into columns [0,256) and [256,512).
-//   warps 16-19 epilogue (TMEM lane quarter = warp % 4).  gate_up: gate and up
-//               rows of one h column sit 8 lanes apart, so one lane exchange
-//               pairs them; h = SiLU(g) * u (fp16) is staged in shared memory
-//               and written out as 128-byte rows.  down: y rows (fp32) go
-//               straight to each pair's output row.
+//   warps 16-19 and 23-26: epilogue, two groups of four (TMEM lane quarter =
+//               warp % 4) that take alternate 32-column chunks of the
+//               accumulator, so that it is drained twice as fast (the MMA
+//               waits for the drained accumulator before the next tile).
+//               gate_up: gate and up rows of one h column sit 8 lanes apart,
+//               so one lane exchange pairs them; h = SiLU(g) * u (fp16) is
+//               staged in shared memory (one buffer per group) and written
+//               out as 128-byte rows.  down: y rows (fp32) go straight to
+//               each pair's output row.
 // A weight tile is dequantised once per 512 tokens.  Stages are handed over
 // with mbarriers; every wait is bounded, and a timeout latches PW_ERR_TIMEOUT
 // and unwinds without trapping.  Decisions that named barriers depend on are
@@ -74,11 +78,13 @@ constexpr int NPS = 6;                  // plane-word stages
 constexpr int kDqWarps = 16;            // warps 0-15
 constexpr int kDqThreads = kDqWarps * 32;
 constexpr int kSetThreads = kDqThreads / 2;
-constexpr int kEpiWarp0 = 16;           // warps 16-19
+constexpr int kEpiWarp0 = 16;           // warps 16-19: epilogue group 0
 constexpr int kSchedWarp = 20;
 constexpr int kPlaneWarp = 21;
 constexpr int kMmaWarp = 22;
-constexpr int kThreads = 23 * 32;
+constexpr int kEpiWarp1 = 23;           // warps 23-26: epilogue group 1
+constexpr int kEpiThreads = 256;        // both groups
+constexpr int kThreads = 27 * 32;
 constexpr int kTileRing = 4;
 constexpr int kTileConsumers = 4;       // dequant, epilogue, plane producer, MMA issuer
 constexpr uint32_t kAStage = BM * BK * 2;     // 8 KB
@@ -248,8 +254,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Both epilogue groups (tile ids and the accumulator flag).
 __device__ __forceinline__ void named_sync_epi() {
-  asm volatile("bar.sync 2, 128;" ::: "memory");
+  asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
+}
+
+// One epilogue group (its staging buffer): barrier 3 or 4.
+__device__ __forceinline__ void named_sync_epi_group(int group) {
+  if (group)
+    asm volatile("bar.sync 4, 128;" ::: "memory");
+  else
+    asm volatile("bar.sync 3, 128;" ::: "memory");
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -481,16 +496,15 @@ __device__ __forceinline__ void dequant_tile(const GemmArgs& a, Mode mode, const
 // L ^ 8 hold the gate and up rows of h column 16q + 8(L / 16) + L % 8; the
 // gate lane finishes the even tokens, the up lane the odd ones.
 __device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, int ntok,
-                                uint32_t tmem_base, int quarter, int lane, int tid_e,
-                                uint32_t sbase, uint32_t& chunk_seq) {
+                                uint32_t tmem_base, int quarter, int lane, int group,
+                                int tid_g, uint32_t sbase) {
   const int up = (lane >> 3) & 1;
   const int hc = 16 * quarter + 8 * (lane >> 4) + (lane & 7);
-  for (int c = 0; c < BN / 32; ++c) {
+  const uint32_t buf = sbase + kOffStage + group * kStageBuf;
+  for (int c = group; c < BN / 32; c += 2) {
     if (c * 32 >= ntok) break;
     float v[32];
     tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
-    const uint32_t buf = sbase + kOffStage + (chunk_seq & 1u) * kStageBuf;
-    ++chunk_seq;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const float send = up ? v[2 * j] : v[2 * j + 1];
@@ -501,10 +515,10 @@ __device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, i
       const int tok = 2 * j + up;
       st_shared_u16(buf + (tok * 64 + hc) * 2, __half_as_ushort(__float2half_rn(h)));
     }
-    named_sync_epi();
+    named_sync_epi_group(group);   // the chunk is staged
 #pragma unroll
     for (int k2 = 0; k2 < 2; ++k2) {
-      const int piece = tid_e + 128 * k2, tok = piece >> 3, part = piece & 7;
+      const int piece = tid_g + 128 * k2, tok = piece >> 3, part = piece & 7;
       const int n = c * 32 + tok;
       if (n < ntok) {
         uint4 val;
@@ -515,6 +529,7 @@ __device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, i
                                   part * 8) = val;
       }
     }
+    named_sync_epi_group(group);   // the buffer is free for the group's next chunk
   }
 }
 
@@ -522,9 +537,9 @@ __device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, i
 // stores for one token are one 128-byte line.  Tiles of an expert that cannot
 // be computed write zeros.
 __device__ void epilogue_down(const GemmArgs& a, const Tile& tile, int pos0, int ntok, bool usable,
-                              uint32_t tmem_base, int quarter, int lane) {
+                              uint32_t tmem_base, int quarter, int lane, int group) {
   const int row = tile.m * BM + quarter * 32 + lane;
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = group; c < BN / 32; c += 2) {
     if (c * 32 >= ntok) break;
     float v[32];
     if (usable) {
@@ -591,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_base + 8 * (kBarTileEmpty + i), kTileConsumers);
     }
     mbar_init(bar_base + 8 * kBarAccFull, 1);
-    mbar_init(bar_base + 8 * kBarAccEmpty, 128);
+    mbar_init(bar_base + 8 * kBarAccEmpty, kEpiThreads);
     mbar_init(bar_base + 8 * kBarFinal, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -630,11 +645,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       it_base += ksteps;
     }
-  } else if (warp < kSchedWarp) {
-    // ---- epilogue
-    const int quarter = warp & 3, tid_e = tid - kEpiWarp0 * 32;
+  } else if (warp < kSchedWarp || warp >= kEpiWarp1) {
+    // ---- epilogue: group 0 = warps 16-19, group 1 = warps 23-26
+    const int group = warp >= kEpiWarp1 ? 1 : 0;
+    const int quarter = warp & 3;
+    const int tid_g = tid - (group ? kEpiWarp1 : kEpiWarp0) * 32;   // 0-127 in the group
+    const int tid_e = tid_g + 128 * group;                           // 0-255
     volatile int* acc_ok = reinterpret_cast<volatile int*>(misc + 10);
-    uint32_t acc_it = 0, seq = 0, iter = 0, chunk_seq = 0;
+    uint32_t acc_it = 0, seq = 0, iter = 0;
     for (;; ++iter) {
       if (tid_e == 0) epi_slot[iter & 1] = ring_take(bar_base, ring, seq, abort, a.status);
       named_sync_epi();
@@ -646,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool usable = tile_usable(mode, a, tile.e);
       if (!usable) {
         if (tid_e == 0) report_unusable(mode, a, tile.e);
-        if (mode == kDown) epilogue_down(a, tile, pos0, ntok, false, tmem_base, quarter, lane);
+        if (mode == kDown) epilogue_down(a, tile, pos0, ntok, false, tmem_base, quarter, lane, group);
         continue;
       }
       if (tid_e == 0)
@@ -656,9 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!*acc_ok) break;
       tc_fence_after();
       if (mode == kGateUp)
-        epilogue_gateup(a, tile, pos0, ntok, tmem_base, quarter, lane, tid_e, sbase, chunk_seq);
+        epilogue_gateup(a, tile, pos0, ntok, tmem_base, quarter, lane, group, tid_g, sbase);
       else
-        epilogue_down(a, tile, pos0, ntok, true, tmem_base, quarter, lane);
+        epilogue_down(a, tile, pos0, ntok, true, tmem_base, quarter, lane, group);
       tc_fence_before();
       mbar_arrive(bar_base + 8 * kBarAccEmpty);
     }
