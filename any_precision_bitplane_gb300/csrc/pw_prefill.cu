@@ -856,19 +856,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ ids,
                                                       const float* __restrict__ wts, int T, int k,
                                                       int E, int H, float* __restrict__ out) {
-  const long long total = static_cast<long long>(T) * H;
+  // four consecutive columns per thread (H is a multiple of 32); a row's
+  // ids and weights are shared by its threads (L1 hits)
+  const int H4 = H / 4;
+  const long long total = static_cast<long long>(T) * H4;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(i / H);
-    const int n = static_cast<int>(i % H);
-    float acc = 0.f;
+    const int t = static_cast<int>(i / H4);
+    const int c4 = static_cast<int>(i - static_cast<long long>(t) * H4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
       const int p = t * k + j;
-      const int e = ids[p];
+      const int e = __ldg(ids + p);
       if (e < 0 || e >= E) continue;
-      acc = fmaf(wts[p], y_ws[static_cast<long long>(p) * H + n], acc);
+      const float w = __ldg(wts + p);
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(y_ws + static_cast<long long>(p) * H) + c4);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
     }
-    out[i] = acc;
+    reinterpret_cast<float4*>(out)[i] = acc;
   }
 }
 
@@ -1070,7 +1078,7 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   g.tile_counter = w.counters + 1;
   dq_gemm_kernel<kDown><<<grid, kThreads, kSmemBytes, stream>>>(g, map_h, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const long long cwork = static_cast<long long>(la.T) * la.H;
+  const long long cwork = static_cast<long long>(la.T) * (la.H / 4);
   const int cblocks = static_cast<int>(std::min<long long>((cwork + 255) / 256, 152LL * 32));
   combine_kernel<<<cblocks, 256, 0, stream>>>(w.y, la.topk_ids, la.topk_weights, la.T, la.k, la.E,
                                               la.H, la.out);
