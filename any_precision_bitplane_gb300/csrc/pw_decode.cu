@@ -133,6 +133,7 @@ struct DecodeWs {
   int* arrive;     // [H/32]   per 64-row range: down tiles finished
   int* gu_done;    // [E]      gate_up tiles finished per expert (released by a fence)
   int heavy_min;   // experts with at least this many pairs are left to the GEMM kernels (0: none)
+  int early_next;  // 1: the down grid leaves SM slots free, so it lets the next launch start early
 };
 
 // Rows streamed by one pass: lane L of row slot g owns row
@@ -713,6 +714,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArg
                                                                   const DecodeWs w,
                                                                   const BitConsts bc) {
   const SmemPtrs s = carve(g_dsmem);
+  // with SM slots to spare, the next call's prep (launched early in that
+  // case) may become resident now and wait for this grid to finish
+  if (w.early_next) allow_dependent_launch();
   // Routing (from the prep launch, which finished before the gate_up
   // kernel allowed this launch) is readable now; h only after the wait.
   const int n_routed = w.ctl[0];
@@ -802,6 +806,10 @@ __device__ __forceinline__ int q_class(int q) {
 // not matter), counters reset.  Other CTAs: hidden -> fp32 and out = 0.
 __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerArgs a,
                                                                    const DecodeWs w) {
+  // when launched early (programmatic dependent launch), nothing of the
+  // previous kernel on the stream (which may be an earlier call still reading
+  // this workspace and writing `out`) is touched before it completes
+  if (w.early_next) grid_dependency_wait();
   allow_dependent_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (blockIdx.x != 0) {
@@ -995,9 +1003,12 @@ int sm_count() {
   return n;
 }
 
-template <typename Kernel>
+// A launch that may start while the previous kernel on the stream finishes
+// (programmatic dependent launch); the kernel waits for it with
+// griddepcontrol.wait before it depends on its results.
+template <typename Kernel, typename... Args>
 cudaError_t launch_dependent(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                             const LayerArgs& a, const DecodeWs& w, const BitConsts& bc) {
+                             const Args&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -1008,7 +1019,7 @@ cudaError_t launch_dependent(Kernel kernel, dim3 grid, dim3 block, size_t smem, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a, w, bc);
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // Some expert can hold kHeavyMinTokens pairs (an expert takes at most one
@@ -1060,6 +1071,11 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
   w.gu_done = reinterpret_cast<int*>(p); p += z.gu_done;
   const bool heavy = hybrid && hybrid_possible(shape);
   w.heavy_min = heavy ? kHeavyMinTokens : 0;
+  // grids: at most one tile per resident CTA (2 per SM)
+  const int slots = a.E < n_pairs ? a.E : n_pairs;
+  const int resident = 2 * sm_count();
+  const int gu_tiles = slots * (a.I / kPairsPerTile);
+  const int dn_tiles = slots * ((a.H + kDownRows - 1) / kDownRows);
 
   const size_t prep_smem = sizeof(int) * static_cast<size_t>(a.E) * (3 + kPrepWarps);
   if (prep_smem > 48 * 1024) {
@@ -1071,18 +1087,26 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
   const long long n4 = static_cast<long long>(a.T) * a.H / 4;
   const long long conv = (n4 + kPrepThreads - 1) / kPrepThreads;
   const int prep_grid = 1 + static_cast<int>(conv < 4 * 152 ? conv : 4 * 152);
-  decode_prep_kernel<<<prep_grid, kPrepThreads, prep_smem, stream>>>(a, w);
-  cudaError_t e = cudaGetLastError();
+  // Small calls (the down grid leaves SM slots free) launch the prep early
+  // and let the down grid release it: it becomes resident while the previous
+  // call's down grid runs and starts the moment that grid completes.
+  // Larger calls gain nothing from it (every slot is busy) and launch it
+  // plainly.  Either way the prep waits for the previous kernel first.
+  w.early_next = dn_tiles < resident ? 1 : 0;
+  cudaError_t e;
+  if (w.early_next) {
+    e = launch_dependent(decode_prep_kernel, dim3(prep_grid), dim3(kPrepThreads), prep_smem,
+                         stream, a, w);
+  } else {
+    decode_prep_kernel<<<prep_grid, kPrepThreads, prep_smem, stream>>>(a, w);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   if (heavy) {
     e = launch_heavy(a, w.offsets, w.perm, w.y, p, kHeavyMinTokens, stream);
     if (e != cudaSuccess) return e;
   }
 
-  const int slots = a.E < n_pairs ? a.E : n_pairs;
-  const int resident = 2 * sm_count();
-  const int gu_tiles = slots * (a.I / kPairsPerTile);
-  const int dn_tiles = slots * ((a.H + kDownRows - 1) / kDownRows);
   const BitConsts bc = make_bit_consts();
   if ((e = record_timing(g_timing.before, stream)) != cudaSuccess) return e;
   e = launch_dependent(decode_gateup_kernel, dim3(gu_tiles < resident ? gu_tiles : resident),
