@@ -39,7 +39,10 @@
  *   - Errors found on the device (an expert id out of range, a page that is
  *     not GPU-resident) never trap: the offending unit of work is skipped and
  *     the first such code is latched in the page table's status word, read
- *     with pw_page_table_status().
+ *     with pw_page_table_status().  Every device-side wait of the forward
+ *     kernels (mbarrier waits in the tcgen05 kernels, the decode down
+ *     kernel's wait for an expert's gate_up tiles) is bounded; one that runs
+ *     out latches PW_ERR_TIMEOUT and the kernel returns.
  */
 #ifndef PW_H_
 #define PW_H_
