@@ -130,6 +130,8 @@ struct GemmArgs {
   const int32_t* perm;      // [n_pairs]
   __half* h_ws;             // [n_pairs][I] (gate_up writes, down reads through TMA)
   float* y_ws;              // [n_pairs][H]
+  float* y_ws2;             // [n_pairs][H]: the second K half's partial sums (ksplit 2)
+  int32_t ksplit;           // 1, or 2: each weight tile's K is split over two tiles
   int32_t* tile_counter;    // zeroed by the gather launch
   int32_t min_tokens;       // experts with fewer pairs get no tiles
   int32_t* status;
@@ -297,16 +299,29 @@ __device__ void drain_copies(uint32_t bar_base, int first, int n, uint32_t seq_e
 
 struct Tile {
   int e, m, n;  // expert, row tile, token tile
+  int kh;       // K part (0, or 1 of 2 when the K range is split)
 };
+
+// The k-steps [k0, k0 + kc) of a tile: the whole K range, or one half of it.
+struct KRange {
+  int k0, kc;
+};
+
+__device__ __forceinline__ KRange k_range(const Tile& tile, int ksteps, int ksplit) {
+  if (ksplit == 1) return KRange{0, ksteps};
+  const int h = ksteps / 2;
+  return tile.kh ? KRange{h, ksteps - h} : KRange{0, h};
+}
 
 __device__ __forceinline__ int m_tiles(Mode mode, const GemmArgs& a) {
   return mode == kGateUp ? a.I / 64 : a.H / BM;
 }
 
-// Tile t of the list ordered (expert, row tile, token tile), token tile
-// fastest (the token tiles of one weight tile run side by side, so the
+// Tile t of the list ordered (expert, row tile, K part, token tile), token
+// tile fastest (the token tiles of one weight tile run side by side, so the
 // second read of its planes is an L2 hit).
-__device__ __forceinline__ Tile tile_at(int t, const int* prefix, int E, const int32_t* offsets) {
+__device__ __forceinline__ Tile tile_at(int t, const int* prefix, int E, const int32_t* offsets,
+                                        int ksplit) {
   int lo = 0, hi = E;  // find e with prefix[e] <= t < prefix[e+1]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -317,8 +332,9 @@ __device__ __forceinline__ Tile tile_at(int t, const int* prefix, int E, const i
   const int nt = (offsets[e + 1] - offsets[e] + BN - 1) / BN;
   Tile r;
   r.e = e;
-  r.m = local / nt;
   r.n = local % nt;
+  r.kh = (local / nt) % ksplit;
+  r.m = local / (nt * ksplit);
   return r;
 }
 
@@ -539,6 +555,7 @@ __device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, i
 __device__ void epilogue_down(const GemmArgs& a, const Tile& tile, int pos0, int ntok, bool usable,
                               uint32_t tmem_base, int quarter, int lane, int group) {
   const int row = tile.m * BM + quarter * 32 + lane;
+  float* const y = tile.kh ? a.y_ws2 : a.y_ws;   // each K part's partial sums
   for (int c = group; c < BN / 32; c += 2) {
     if (c * 32 >= ntok) break;
     float v[32];
@@ -553,7 +570,7 @@ __device__ void epilogue_down(const GemmArgs& a, const Tile& tile, int pos0, int
       const int n = c * 32 + j;
       if (n < ntok) {
         const int pair = a.perm[pos0 + n];
-        a.y_ws[static_cast<long long>(pair) * a.H + row] = v[j];
+        y[static_cast<long long>(pair) * a.H + row] = v[j];
       }
     }
   }
@@ -578,6 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int mt = m_tiles(mode, a);
   const int K = (mode == kGateUp) ? a.H : a.I;
   const int ksteps = K / BK;
+  // gate_up tiles always take the whole K range (a compile-time 1 here keeps
+  // that instantiation free of the split's index arithmetic)
+  const int ksplit = (mode == kGateUp) ? 1 : a.ksplit;
   if (sbase & 1023u) {   // the swizzled stages need a 1024-byte aligned base
     if (tid == 0) latch_status(a.status, PW_ERR_CUDA);
     return;
@@ -589,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = 0; e < a.E; ++e) {
       prefix[e] = run;
       const int cnt = a.offsets[e + 1] - a.offsets[e];
-      if (cnt >= a.min_tokens) run += mt * ((cnt + BN - 1) / BN);
+      if (cnt >= a.min_tokens) run += mt * ksplit * ((cnt + BN - 1) / BN);
     }
     prefix[a.E] = run;
     for (int i = 0; i < NST; ++i) {
@@ -632,18 +652,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_sync_dq();   // the previous tile's lookups are done; the tile id is visible
       const int t = dq_slot[iter & 1];
       if (t >= total) break;
-      const Tile tile = tile_at(t, prefix, a.E, a.offsets);
+      const Tile tile = tile_at(t, prefix, a.E, a.offsets, ksplit);
       if (!tile_usable(mode, a, tile.e)) continue;
       const pw_block_entry ent = a.table[2 * tile.e + (mode == kGateUp ? 0 : 1)];
       const DqRow d = dq_row(mode, a, tile.m, w, lane);
+      const int kc = k_range(tile, ksteps, ksplit).kc;
       switch (ent.q) {
-        case 3: dequant_tile<3>(a, mode, ent, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc); break;
-        case 4: dequant_tile<4>(a, mode, ent, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc); break;
-        case 5: dequant_tile<5>(a, mode, ent, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc); break;
-        case 6: dequant_tile<6>(a, mode, ent, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc); break;
-        default: dequant_tile<8>(a, mode, ent, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc); break;
+        case 3: dequant_tile<3>(a, mode, ent, d, kc, it_base, set, half, sbase, bar_base, abort, bc); break;
+        case 4: dequant_tile<4>(a, mode, ent, d, kc, it_base, set, half, sbase, bar_base, abort, bc); break;
+        case 5: dequant_tile<5>(a, mode, ent, d, kc, it_base, set, half, sbase, bar_base, abort, bc); break;
+        case 6: dequant_tile<6>(a, mode, ent, d, kc, it_base, set, half, sbase, bar_base, abort, bc); break;
+        default: dequant_tile<8>(a, mode, ent, d, kc, it_base, set, half, sbase, bar_base, abort, bc); break;
       }
-      it_base += ksteps;
+      it_base += kc;
     }
   } else if (warp < kSchedWarp || warp >= kEpiWarp1) {
     // ---- epilogue: group 0 = warps 16-19, group 1 = warps 23-26
@@ -658,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_sync_epi();
       const int t = epi_slot[iter & 1];
       if (t >= total) break;
-      const Tile tile = tile_at(t, prefix, a.E, a.offsets);
+      const Tile tile = tile_at(t, prefix, a.E, a.offsets, ksplit);
       const int pos0 = a.offsets[tile.e] + tile.n * BN;
       const int ntok = min(BN, a.offsets[tile.e + 1] - pos0);
       const bool usable = tile_usable(mode, a, tile.e);
@@ -694,13 +715,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ring[slot] = t;
         mbar_arrive(bar_base + 8 * (kBarTileFull + slot));
         if (t == INT_MAX) break;
-        const Tile tile = tile_at(t, prefix, a.E, a.offsets);
+        const Tile tile = tile_at(t, prefix, a.E, a.offsets, ksplit);
         if (!tile_usable(mode, a, tile.e)) continue;
         const int pos0 = a.offsets[tile.e] + tile.n * BN;
         const int ntok = min(BN, a.offsets[tile.e + 1] - pos0);
         const int halves = ntok > BNH ? 2 : 1;
+        const KRange kr = k_range(tile, ksteps, ksplit);
         bool ok = true;
-        for (int s = 0; s < ksteps; ++s, ++it) {
+        for (int s = 0; s < kr.kc; ++s, ++it) {
           const uint32_t stage = it % NST, spar = (it / NST) & 1u;
           if (!mbar_wait(bar_base + 8 * (kBarEmpty + stage), spar ^ 1u, abort, a.status)) {
             ok = false;
@@ -709,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t full = bar_base + 8 * (kBarFullB + stage);
           mbar_arrive_tx(full, halves * kBHalf);
           for (int h = 0; h < halves; ++h)
-            tma_load_2d(sbase + kOffB + stage * kBStage + h * kBHalf, &tmap_b, s * BK,
+            tma_load_2d(sbase + kOffB + stage * kBStage + h * kBHalf, &tmap_b, (kr.k0 + s) * BK,
                         pos0 + h * BNH, full);
         }
         if (!ok) break;
@@ -729,15 +751,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) t0 = ring_take(bar_base, ring, seq, abort, a.status);
         const int t = __shfl_sync(0xffffffffu, t0, 0);
         if (t >= total) break;
-        const Tile tile = tile_at(t, prefix, a.E, a.offsets);
+        const Tile tile = tile_at(t, prefix, a.E, a.offsets, ksplit);
         if (!tile_usable(mode, a, tile.e)) continue;
         const pw_block_entry ent = a.table[2 * tile.e + (mode == kGateUp ? 0 : 1)];
         const int q = ent.q;
         const uint32_t* base =
             ent.planes + ((mode == kGateUp) ? static_cast<long long>(tile.m) * 64
                                             : static_cast<long long>(tile.m) * BM);
+        const KRange kr = k_range(tile, ksteps, ksplit);
         bool ok = true;
-        for (int s = 0; s < ksteps; ++s, ++pit) {
+        for (int s = 0; s < kr.kc; ++s, ++pit) {
           const uint32_t ps = pit % NPS, pp = (pit / NPS) & 1u;
           int ok0 = 1;
           if (lane == 0) ok0 = mbar_wait(bar_base + 8 * (kBarPlEmpty + ps), pp ^ 1u, abort, a.status);
@@ -749,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dst = sbase + kOffPlanes + ps * kPlaneStage + lane * 16;
           // lane L copies 16 bytes of each plane: words 4L..4L+3 of the
           // stage slab (gate_up: lanes 0-15 the gate run, 16-31 the up run)
-          const uint32_t* src = base + static_cast<long long>(s) * N +
+          const uint32_t* src = base + static_cast<long long>(kr.k0 + s) * N +
                                 ((mode == kGateUp) ? ((lane >> 4) * a.I + (lane & 15) * 4) : lane * 4);
           for (int p = 0; p < q; ++p) cp_async16(dst + p * 512, src + p * plane_stride);
           cp_async_arrive(full);
@@ -766,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (;;) {
         const int t = ring_take(bar_base, ring, seq, abort, a.status);
         if (t >= total) break;
-        const Tile tile = tile_at(t, prefix, a.E, a.offsets);
+        const Tile tile = tile_at(t, prefix, a.E, a.offsets, ksplit);
         if (!tile_usable(mode, a, tile.e)) continue;
         const int pos0 = a.offsets[tile.e] + tile.n * BN;
         const int ntok = min(BN, a.offsets[tile.e + 1] - pos0);
@@ -775,8 +798,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t id0 = make_idesc(n0), id1 = make_idesc(n1 > 0 ? n1 : 16);
         if (!mbar_wait(bar_base + 8 * kBarAccEmpty, (acc_it & 1u) ^ 1u, abort, a.status)) break;
         tc_fence_after();
+        const int kc = k_range(tile, ksteps, ksplit).kc;
         bool ok = true;
-        for (int s = 0; s < ksteps; ++s, ++it) {
+        for (int s = 0; s < kc; ++s, ++it) {
           const uint32_t stage = it % NST, par = (it / NST) & 1u;
           if (!mbar_wait(bar_base + 8 * (kBarFullA + stage), par, abort, a.status) ||
               !mbar_wait(bar_base + 8 * (kBarFullB + stage), par, abort, a.status)) {
@@ -853,11 +877,13 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
 }
 
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y_ws,
+                                                      const float* __restrict__ y_ws2,
                                                       const int32_t* __restrict__ ids,
                                                       const float* __restrict__ wts, int T, int k,
                                                       int E, int H, float* __restrict__ out) {
   // four consecutive columns per thread (H is a multiple of 32); a row's
-  // ids and weights are shared by its threads (L1 hits)
+  // ids and weights are shared by its threads (L1 hits).  With y_ws2 the
+  // down GEMM split K in two: a pair's row is the sum of its two parts.
   const int H4 = H / 4;
   const long long total = static_cast<long long>(T) * H4;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -870,7 +896,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       const int e = __ldg(ids + p);
       if (e < 0 || e >= E) continue;
       const float w = __ldg(wts + p);
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(y_ws + static_cast<long long>(p) * H) + c4);
+      float4 v = __ldcs(reinterpret_cast<const float4*>(y_ws + static_cast<long long>(p) * H) + c4);
+      if (y_ws2) {
+        const float4 v2 =
+            __ldcs(reinterpret_cast<const float4*>(y_ws2 + static_cast<long long>(p) * H) + c4);
+        v.x += v2.x;
+        v.y += v2.y;
+        v.z += v2.z;
+        v.w += v2.w;
+      }
       acc.x = fmaf(w, v.x, acc.x);
       acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z);
@@ -891,6 +925,7 @@ struct WsLayout {
   __half* xg;
   __half* h;
   float* y;
+  float* y2;   // the down GEMM's second K half
 };
 
 WsLayout carve_ws(void* ws, const pw_moe_shape& s) {
@@ -908,6 +943,8 @@ WsLayout carve_ws(void* ws, const pw_moe_shape& s) {
   w.h = reinterpret_cast<__half*>(p);
   p += round256(2 * P * s.I);
   w.y = reinterpret_cast<float*>(p);
+  p += round256(4 * P * s.H);
+  w.y2 = reinterpret_cast<float*>(p);
   return w;
 }
 
@@ -1002,6 +1039,8 @@ cudaError_t launch_heavy(const LayerArgs& la, const int32_t* offsets, const int3
   g.perm = perm;
   g.h_ws = h;
   g.y_ws = y;
+  g.y_ws2 = nullptr;
+  g.ksplit = 1;   // the decode path's combine reads one y
   g.status = la.status;
   g.min_tokens = min_tokens;
   const int grid = num_sms();
@@ -1017,7 +1056,7 @@ cudaError_t launch_heavy(const LayerArgs& la, const int32_t* offsets, const int3
 size_t prefill_workspace_bytes(const pw_moe_shape& s) {
   const size_t P = static_cast<size_t>(s.T) * s.k;
   return 256 + round256(sizeof(int32_t) * (s.E + 1)) + round256(sizeof(int32_t) * P) +
-         round256(2 * P * s.H) + round256(2 * P * s.I) + round256(4 * P * s.H);
+         round256(2 * P * s.H) + round256(2 * P * s.I) + 2 * round256(4 * P * s.H);
 }
 
 bool prefill_shape_ok(const pw_moe_shape& s) {
@@ -1066,6 +1105,8 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   g.perm = w.perm;
   g.h_ws = w.h;
   g.y_ws = w.y;
+  g.y_ws2 = w.y2;
+  g.ksplit = 1;
   g.status = la.status;
   g.min_tokens = 1;
   const int grid = num_sms();
@@ -1075,13 +1116,18 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   dq_gemm_kernel<kGateUp><<<grid, kThreads, kSmemBytes, stream>>>(g, map_x, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = record_timing(g_timing.after, stream)) != cudaSuccess) return e;
+  // The down GEMM has H/128 row tiles per expert, too few to fill the SMs
+  // evenly (a Mixtral-shaped call: 512 tiles on 152 SMs, 3.4 rounds); its K
+  // (= I) is long, so each weight tile's K range is split over two tiles
+  // whose partial sums land in y and y2 and meet in the combine.
   g.tile_counter = w.counters + 1;
+  g.ksplit = (la.I / BK >= 2) ? 2 : 1;
   dq_gemm_kernel<kDown><<<grid, kThreads, kSmemBytes, stream>>>(g, map_h, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long cwork = static_cast<long long>(la.T) * (la.H / 4);
   const int cblocks = static_cast<int>(std::min<long long>((cwork + 255) / 256, 152LL * 32));
-  combine_kernel<<<cblocks, 256, 0, stream>>>(w.y, la.topk_ids, la.topk_weights, la.T, la.k, la.E,
-                                              la.H, la.out);
+  combine_kernel<<<cblocks, 256, 0, stream>>>(w.y, g.ksplit == 2 ? w.y2 : nullptr, la.topk_ids,
+                                              la.topk_weights, la.T, la.k, la.E, la.H, la.out);
   return cudaGetLastError();
 }
 
