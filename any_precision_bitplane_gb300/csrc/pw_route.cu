@@ -64,14 +64,17 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   }
 }
 
-// Single CTA of 8 warps.  Pass 1 counts pairs per expert; a block scan turns
-// the counts into offsets.  Pass 2 walks the pairs in chunks of 256 in
-// ascending order: inside a warp, __match_any_sync gives each pair its rank
-// among same-expert lanes; per-warp counts in shared memory give the rank
-// among earlier warps of the chunk; a running base per expert carries the
-// count of earlier chunks.  Position = offsets[e] + earlier pairs of e, which
-// is the stable order.
-constexpr int kPermThreads = 256;
+// Single CTA of 32 warps; warp w owns the contiguous run of pairs
+// [w*L, (w+1)*L), L = ceil(n_pairs / 32).  Pass 1: each warp counts its
+// pairs per expert (__match_any_sync groups same-expert lanes; the group's
+// first lane adds the group size to the warp's own row of counts, so no
+// atomics).  Then thread e turns column e of the counts into the expert's
+// running start per warp, and a block scan of the per-expert totals gives
+// offsets.  Pass 2: each warp walks its run again and places every pair at
+// its warp's running start for the expert plus its rank among same-expert
+// lanes of the step.  Runs are in pair order and ranks follow lane order, so
+// the placement is the stable one: position = offsets[e] + earlier pairs of e.
+constexpr int kPermThreads = 1024;
 constexpr int kPermWarps = kPermThreads / 32;
 
 __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __restrict__ ids,
@@ -81,33 +84,38 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
                                                                int32_t* __restrict__ inv,
                                                                int32_t* status) {
   extern __shared__ int smem[];
-  int* s_count = smem;                 // [E]
-  int* s_base = s_count + E;           // [E] running position of the next pair of e
-  int* s_wcnt = s_base + E;            // [kPermWarps][E]
+  int* s_cnt = smem;                   // [kPermWarps][E]: counts, then running starts
   __shared__ int s_warp_sum[kPermWarps];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
+  const int L = (n_pairs + kPermWarps - 1) / kPermWarps;
+  const int lo = min(n_pairs, warp * L), hi = min(n_pairs, lo + L);
 
-  for (int e = tid; e < E; e += kPermThreads) s_count[e] = 0;
-  for (int i = tid; i < kPermWarps * E; i += kPermThreads) s_wcnt[i] = 0;
+  for (int i = tid; i < kPermWarps * E; i += kPermThreads) s_cnt[i] = 0;
   __syncthreads();
-  for (int p = tid; p < n_pairs; p += kPermThreads) {
-    const int e = ids[p];
-    if (e >= 0 && e < E) {
-      atomicAdd(&s_count[e], 1);
-    } else {
-      latch_status(status, PW_ERR_BAD_EXPERT_ID);
-    }
+  int* my = s_cnt + warp * E;
+  for (int base = lo; base < hi; base += 32) {
+    const int p = base + lane;
+    const int e = (p < hi) ? ids[p] : -1;
+    const bool valid = (e >= 0 && e < E);
+    if (p < hi && !valid) latch_status(status, PW_ERR_BAD_EXPERT_ID);
+    const unsigned peers = __match_any_sync(kFull, valid ? e : -1);
+    if (valid && (peers & ((1u << lane) - 1u)) == 0) my[e] += __popc(peers);
   }
   __syncthreads();
 
-  // Exclusive scan of s_count into s_base: each thread owns a contiguous run.
-  const int per = (E + kPermThreads - 1) / kPermThreads;
-  const int lo = min(E, tid * per), hi = min(E, lo + per);
-  int run = 0;
-  for (int e = lo; e < hi; ++e) run += s_count[e];
-  int incl = run;
+  // column e: per-warp exclusive prefix (in place) and the expert's total
+  int tot = 0;
+  if (tid < E) {
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int c = s_cnt[w * E + tid];
+      s_cnt[w * E + tid] = tot;
+      tot += c;
+    }
+  }
+  // exclusive block scan of the totals over experts (thread e holds expert e)
+  int incl = tot;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int v = __shfl_up_sync(kFull, incl, off);
@@ -115,12 +123,11 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
   }
   if (lane == 31) s_warp_sum[warp] = incl;
   __syncthreads();
-  int before = incl - run;
+  int before = incl - tot;
   for (int w = 0; w < warp; ++w) before += s_warp_sum[w];
-  for (int e = lo; e < hi; ++e) {
-    s_base[e] = before;
-    offsets[e] = before;
-    before += s_count[e];
+  if (tid < E) {
+    offsets[tid] = before;
+    for (int w = 0; w < kPermWarps; ++w) s_cnt[w * E + tid] += before;
   }
   if (tid == kPermThreads - 1) {
     int total = 0;
@@ -129,33 +136,21 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
   }
   __syncthreads();
 
-  for (int c0 = 0; c0 < n_pairs; c0 += kPermThreads) {
-    const int p = c0 + tid;
-    const int e = (p < n_pairs) ? ids[p] : -1;
+  for (int base = lo; base < hi; base += 32) {
+    const int p = base + lane;
+    const int e = (p < hi) ? ids[p] : -1;
     const bool valid = (e >= 0 && e < E);
-    const int key = valid ? e : -1;
-    const unsigned peers = __match_any_sync(kFull, key);
+    const unsigned peers = __match_any_sync(kFull, valid ? e : -1);
     const unsigned lower = peers & ((1u << lane) - 1u);
-    if (valid && lower == 0) s_wcnt[warp * E + e] = __popc(peers);
-    __syncthreads();
+    int pos = -1;
     if (valid) {
-      int pos = s_base[e] + __popc(lower);
-      for (int w = 0; w < warp; ++w) pos += s_wcnt[w * E + e];
+      pos = my[e] + __popc(lower);
       perm[pos] = p;
-      if (inv != nullptr) inv[p] = pos;
-    } else if (p < n_pairs && inv != nullptr) {
-      inv[p] = -1;
     }
-    __syncthreads();
-    for (int x = tid; x < E; x += kPermThreads) {
-      int add = 0;
-      for (int w = 0; w < kPermWarps; ++w) {
-        add += s_wcnt[w * E + x];
-        s_wcnt[w * E + x] = 0;
-      }
-      s_base[x] += add;
-    }
-    __syncthreads();
+    if (p < hi && inv != nullptr) inv[p] = pos;
+    __syncwarp();   // every lane has read its start before the group's first lane moves it
+    if (valid && lower == 0) my[e] += __popc(peers);
+    __syncwarp();
   }
 }
 
@@ -171,7 +166,7 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
 
 cudaError_t launch_permute(const int32_t* ids, int n_pairs, int E, int32_t* offsets,
                            int32_t* perm, int32_t* inv, int32_t* status, cudaStream_t s) {
-  const size_t smem = sizeof(int) * static_cast<size_t>(E) * (2 + kPermWarps);
+  const size_t smem = sizeof(int) * static_cast<size_t>(E) * kPermWarps;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
