@@ -72,6 +72,20 @@ def test_permute_skewed_routing(pw):
     np.testing.assert_array_equal(perm.cpu().numpy(), r_perm)
 
 
+def test_permute_long_runs_per_warp(pw):
+    # 40000 pairs: every warp of the permute CTA walks ~40 steps of 32 pairs,
+    # so each expert's running start carries across many steps; heavy skew
+    # puts up to 32 lanes of one step on the same expert
+    rng = np.random.default_rng(11)
+    ids = np.where(rng.random((20000, 2)) < 0.5, rng.integers(0, 3, (20000, 2)),
+                   rng.integers(0, 64, (20000, 2))).astype(np.int32)
+    off, perm, inv = pw.permute(torch.from_numpy(ids).cuda(), 64)
+    r_off, r_perm, r_inv = moe.permute(ids, 64)
+    np.testing.assert_array_equal(off.cpu().numpy(), r_off)
+    np.testing.assert_array_equal(perm.cpu().numpy(), r_perm)
+    np.testing.assert_array_equal(inv.cpu().numpy(), r_inv)
+
+
 def test_permute_empty(pw):
     ids = torch.zeros((0, 2), dtype=torch.int32, device="cuda")
     off, perm, inv = pw.permute(ids, 5)
