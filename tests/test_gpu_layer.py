@@ -159,3 +159,33 @@ def test_workspace_too_small_is_rejected(pw):
         pw.moe_forward(hidden, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(),
                        dl.table, dl.I, dl.E, workspace=ws)
     assert ei.value.code == pw.PW_ERR_WORKSPACE
+
+
+def test_back_to_back_calls_of_mixed_sizes_share_one_workspace(pw):
+    # Calls of different sizes queued on one stream with no host sync between
+    # them, all on one workspace: small calls (whose down grid leaves SM slots
+    # free) launch their grouping kernel early, behind the previous call's
+    # down kernel; large calls launch it plainly.  Every transition must leave
+    # each call's result equal to the oracle's.
+    layer = gen.make_layer(configs.custom("mixed_sizes", 1024, 256, 32, 4, 64), seed=31)
+    dl = device_layer(layer, "mixed_sizes")
+    sizes = [1, 64, 1, 2, 64, 1, 3]
+    ws = torch.empty(max(pw.workspace_bytes(T, dl.H, dl.I, dl.E, 4) for T in sizes),
+                     dtype=torch.uint8, device="cuda")
+    # each call takes its own slice of one token stream, so inputs differ
+    pool = gen.make_tokens(layer, sum(sizes))
+    calls, t0 = [], 0
+    for T in sizes:
+        tok = gen.Tokens(pool.hidden_bf16[t0:t0 + T].copy(), pool.logits[t0:t0 + T].copy())
+        t0 += T
+        ids, w = oracle_route(tok, 4)
+        args = (torch.from_numpy(tok.hidden_bf16.view(np.int16)).cuda(),
+                torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda())
+        calls.append((tok, ids, w, args))
+    torch.cuda.synchronize()
+    outs = [pw.moe_forward(*args, dl.table, dl.I, dl.E, workspace=ws) for _, _, _, args in calls]
+    torch.cuda.synchronize()
+    assert dl.table.status() == pw.PW_OK
+    for (tok, ids, w, _), out in zip(calls, outs):
+        ref = oracle_out(layer, tok.hidden_bf16, ids, w)
+        assert rel_l2(out.cpu().numpy(), ref) <= REL_TOL
