@@ -1022,17 +1022,17 @@ cudaError_t launch_dependent(Kernel kernel, dim3 grid, dim3 block, size_t smem, 
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// Some expert can hold kHeavyMinTokens pairs (an expert takes at most one
-// pair per token) and the GEMM kernels support the shape.
+// The call is large enough for the GEMM launches to pay off and the GEMM
+// kernels support the shape.
 bool hybrid_possible(const pw_moe_shape& s) {
-  return s.T >= kHeavyMinTokens && prefill_shape_ok(s);
+  return s.T >= kHybridMinTokens && prefill_shape_ok(s);
 }
 
 }  // namespace
 
 // Workspace: x32 [T][H] | h [T*k][I] | y [T*k][H] fp32 | offsets [E+1] |
 // perm [T*k] | routed lists [E] x 2 | control words | arrival counters [H/32]
-// | gate_up tiles done [E] | (when some expert can hold kHeavyMinTokens pairs)
+// | gate_up tiles done [E] | (in calls of at least kHybridMinTokens tokens)
 // the GEMM kernels' scratch.
 size_t decode_workspace_bytes(const pw_moe_shape& s, bool hybrid) {
   const WsSizes z = ws_sizes(s);

@@ -81,10 +81,13 @@ struct LayerArgs {
 // Routing statistics of one call (pairs per expert, sum of their weights),
 // added to a.stats_counts / a.stats_mass; no-op when they are NULL.
 cudaError_t launch_routing_stats(const LayerArgs& a, cudaStream_t s);
-// Experts with at least this many pairs in a decode call go through the
-// tensor-core GEMM kernels of the prefill path (when the shape allows it);
-// the others through the decode kernels.
-constexpr int kHeavyMinTokens = 16;
+// In decode calls of at least kHybridMinTokens tokens (when the shape allows
+// it), experts with at least kHeavyMinTokens pairs go through the tensor-core
+// GEMM kernels of the prefill path; the others through the decode kernels,
+// which stream an expert's weights once per group of 4 tokens.  Smaller
+// calls skip the GEMM launches (three of them) altogether.
+constexpr int kHeavyMinTokens = 8;
+constexpr int kHybridMinTokens = 16;
 // `hybrid` = false keeps every expert on the decode kernels (and the
 // workspace free of the GEMM path's buffers).
 size_t decode_workspace_bytes(const pw_moe_shape& s, bool hybrid = true);

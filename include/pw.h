@@ -74,9 +74,10 @@ extern "C" {
 
 /* ---- forward paths ----------------------------------------------------- */
 #define PW_PATH_AUTO     0  /* decode kernels for small token counts, else prefill */
-#define PW_PATH_DECODE   1  /* CUDA-core fused decode kernels; within a call, experts
-                                holding >= 16 pairs go through the tcgen05 GEMM
-                                kernels (when the shape allows them)               */
+#define PW_PATH_DECODE   1  /* CUDA-core fused decode kernels; within a call of
+                                >= 16 tokens, experts holding >= 8 pairs go
+                                through the tcgen05 GEMM kernels (when the shape
+                                allows them)                                        */
 #define PW_PATH_PREFILL  2  /* dequantise-to-shared-memory tcgen05 GEMM kernels     */
 
 /* One linear block's page-table entry (24 bytes).  PagedWeight, "Core
