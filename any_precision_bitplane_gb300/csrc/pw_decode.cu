@@ -10,8 +10,10 @@
 //            the routed experts largest-bitwidth first (so the costliest
 //            tiles are scheduled first) with each one's page-table entry,
 //            and resets the tile counters; the other CTAs widen the hidden
-//            states to fp32 and zero `out`.
-//   [heavy]  experts holding at least kHeavyMinTokens pairs are left out of
+//            states to fp32 and zero `out`.  In small calls it is launched
+//            early too, behind the previous call's down kernel.
+//   [heavy]  in calls of at least kHybridMinTokens tokens, experts holding
+//            at least kHeavyMinTokens pairs are left out of
 //            those lists: the tcgen05 GEMM kernels of the prefill path run
 //            them (gather, gate_up, down -> y) between prep and gate_up, so
 //            their planes are read and dequantised once instead of once per

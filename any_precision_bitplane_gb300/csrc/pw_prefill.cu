@@ -10,9 +10,9 @@
 //   gather     xg[pos] = fp16(hidden[perm[pos] / k])            (one pass)
 //   gate_up    per (expert, 64 gate/up row pairs, 512 tokens):  D = W_gu x^T
 //              in TMEM, epilogue h = SiLU(g) * u -> fp16 h[pos]
-//   down       per (expert, 128 down rows, 512 tokens):         D = W_dn h^T,
-//              epilogue y[pair] (fp32)
-//   combine    out[t] = sum_j w_tj * y[t*k + j], j order        (one pass)
+//   down       per (expert, 128 down rows, 512 tokens, K half): D = W_dn h^T
+//              over one half of K, epilogue y[pair] or y2[pair] (fp32)
+//   combine    out[t] = sum_j w_tj * (y + y2)[t*k + j], j order (one pass)
 //
 // GEMM kernel: one CTA per SM, persistent, 23 warps in five roles.
 //   warp 20     scheduler and token-operand producer: takes tile ids from a
