@@ -836,6 +836,13 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
   const bool stats = a.stats_counts != nullptr;
   __shared__ int s_warp_sum[kPrepWarps];
   __shared__ int s_bucket[2][8];
+  // the page-table entries of this thread's first expert load now, so that
+  // their round trip overlaps the pair counting
+  pw_block_entry t_gu = {}, t_dn = {};
+  if (tid < E) {
+    t_gu = a.table[2 * tid];
+    t_dn = a.table[2 * tid + 1];
+  }
   for (int e = tid; e < E; e += kPrepThreads) {
     count[e] = 0;
     wsum[e] = 0.f;
@@ -892,8 +899,8 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
   const int heavy_min = w.heavy_min > 0 ? w.heavy_min : INT_MAX;
   for (int e = tid; e < E; e += kPrepThreads) {
     if (count[e] > 0 && count[e] < heavy_min) {
-      atomicAdd(&s_bucket[0][q_class(a.table[2 * e].q)], 1);
-      atomicAdd(&s_bucket[1][q_class(a.table[2 * e + 1].q)], 1);
+      atomicAdd(&s_bucket[0][q_class(e == tid ? t_gu.q : a.table[2 * e].q)], 1);
+      atomicAdd(&s_bucket[1][q_class(e == tid ? t_dn.q : a.table[2 * e + 1].q)], 1);
     }
   }
   __syncthreads();
@@ -913,7 +920,8 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
   __syncthreads();
   for (int e = tid; e < E; e += kPrepThreads) {
     if (count[e] > 0 && count[e] < heavy_min) {
-      const pw_block_entry gu = a.table[2 * e], dn = a.table[2 * e + 1];
+      const pw_block_entry gu = e == tid ? t_gu : a.table[2 * e];
+      const pw_block_entry dn = e == tid ? t_dn : a.table[2 * e + 1];
       const bool gu_ok = gu.state == PW_PAGE_GPU && supported_q(gu.q);
       const bool dn_ok = dn.state == PW_PAGE_GPU && supported_q(dn.q);
       SlotInfo si;
