@@ -80,6 +80,7 @@ _SIGNATURES = {
     "pw_planes_from_host": (_c.c_int, [_P, _P, _I32, _I32, _I32, _P]),
     "pw_page_table_commit_after": (_c.c_int, [_P, _I32, _P, _P, _P, _P, _P]),
     "pw_plan_recommit": (_c.c_int, [_I32, _P, _P, _P, _P, _I32, _c.c_int64, _P, _P, _P, _P]),
+    "pw_debug_bounded_wait": (_c.c_int, [_P, _I32, _I32, _P]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -314,6 +315,15 @@ def moe_forward_noalloc(hidden, topk_ids, topk_weights, table, I, E, out=None, s
                                         _ptr(topk_weights), table.handle, _ptr(out),
                                         _stream(stream)), "pw_moe_forward_noalloc")
     return out
+
+
+def debug_bounded_wait(table, which, polls, stream=None):
+    """Run one of the forward kernels' bounded device waits (0: the decode
+    down kernel's wait for gate_up tiles, 1: the tensor-core kernels'
+    mbarrier wait) against something never released, with `polls` as its
+    limit; it latches PW_ERR_TIMEOUT in the table's status word."""
+    _check(lib().pw_debug_bounded_wait(table.handle, int(which), int(polls), _stream(stream)),
+           "pw_debug_bounded_wait")
 
 
 def set_timing_events(before=None, after=None):

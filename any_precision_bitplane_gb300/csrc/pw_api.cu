@@ -1,7 +1,9 @@
 // extern "C" entry points of libpw: argument validation and launches only.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "pw_internal.cuh"
@@ -28,17 +30,18 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // error instead of a launch failure.
 int check_device() {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  static int checked[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
-  if (dev >= 0 && dev < 64 && checked[dev] == 1) return PW_OK;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  static std::atomic<int> checked[kMaxDevices];  // 0 unknown, 1 ok, 2 unsupported
+  if (checked[dev].load(std::memory_order_relaxed) == 1) return PW_OK;
   int major = 0, minor = 0;
+  cudaError_t e;
   if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
     return cuda_fail(e, "cudaDeviceGetAttribute");
   if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
     return cuda_fail(e, "cudaDeviceGetAttribute");
   const bool ok = (major == 10 && minor == 3);
-  if (dev >= 0 && dev < 64) checked[dev] = ok ? 1 : 2;
+  checked[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
   if (!ok)
     return fail(PW_ERR_UNSUPPORTED_DEVICE, "device %d is sm_%d%d; libpw is built for sm_103a", dev,
                 major, minor);
@@ -61,42 +64,19 @@ int check_shape(const pw_moe_shape* s) {
 int forward_impl(const pw_moe_shape* shape, const void* hidden, const int32_t* topk_ids,
                  const float* topk_weights, const pw_page_table* table, float* out,
                  void* workspace, size_t workspace_bytes, int32_t path, cudaStream_t stream) {
-  int rc = check_shape(shape);
-  if (rc) return rc;
-  const pw_moe_shape& s = *shape;
-  if (table == nullptr) return fail(PW_ERR_INVALID_ARG, "table is NULL");
-  if (table->num_blocks != 2 * s.E)
-    return fail(PW_ERR_SHAPE, "page table has %d blocks, shape needs 2E = %d", table->num_blocks,
-                2 * s.E);
   if (path < PW_PATH_AUTO || path > PW_PATH_PREFILL)
     return fail(PW_ERR_INVALID_ARG, "unknown path %d", path);
-  if (s.T == 0) return PW_OK;
-  if (!hidden || !topk_ids || !topk_weights || !out)
-    return fail(PW_ERR_INVALID_ARG, "hidden, topk_ids, topk_weights and out must be non-NULL");
-  if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(topk_ids, 4) ||
-      !aligned(topk_weights, 4))
-    return fail(PW_ERR_INVALID_ARG, "hidden and out must be 16-byte aligned");
-  if ((rc = check_device())) return rc;
+  LayerArgs a;
+  bool empty = false;
+  int rc = check_forward_args(shape, hidden, topk_ids, topk_weights, table, out, &a, &empty);
+  if (rc || empty) return rc;
+  const pw_moe_shape& s = *shape;
   const long long n_pairs = static_cast<long long>(s.T) * s.k;
   if (path == PW_PATH_AUTO) path = (n_pairs >= prefill_min_pairs(s)) ? PW_PATH_PREFILL : PW_PATH_DECODE;
   size_t need = (path == PW_PATH_DECODE) ? decode_workspace_bytes(s) : prefill_workspace_bytes(s);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
     return fail(PW_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes (got %zu)",
                 need, workspace_bytes);
-  LayerArgs a;
-  a.T = s.T;
-  a.H = s.H;
-  a.I = s.I;
-  a.E = s.E;
-  a.k = s.k;
-  a.hidden = static_cast<const uint16_t*>(hidden);
-  a.topk_ids = topk_ids;
-  a.topk_weights = topk_weights;
-  a.table = table->d_entries;
-  a.out = out;
-  a.status = table->d_status;
-  a.stats_counts = table->stats_counts;
-  a.stats_mass = table->stats_mass;
   cudaError_t e;
   if (path == PW_PATH_DECODE) {
     if (n_pairs > decode_max_pairs() || s.E > decode_max_experts())
@@ -129,8 +109,9 @@ int update_table(pw_page_table* t, int32_t n, const int32_t* ids, int kind, cons
       return fail(PW_ERR_INVALID_ARG, "entry %d: pointer NULL or not 16-byte aligned", i);
   }
   int cur = 0;
-  cudaError_t e = cudaGetDevice(&cur);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int rc = current_device(&cur);
+  if (rc) return rc;
+  cudaError_t e;
   if (cur != t->device)
     return fail(PW_ERR_INVALID_ARG, "current device %d is not the table's device %d", cur,
                 t->device);
@@ -164,6 +145,85 @@ int cuda_fail(cudaError_t err, const char* what) {
 }
 
 void clear_error() { g_err[0] = 0; }
+
+int current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices)
+    return fail(PW_ERR_INVALID_ARG, "device ordinal %d outside 0..%d", *dev, kMaxDevices - 1);
+  return PW_OK;
+}
+
+int sm_count() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+cudaError_t setup_once(SetupKey key, cudaError_t (*fn)()) {
+  static std::atomic<bool> done[kMaxDevices][kSetupKeys];
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (done[dev][key].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev][key].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = fn();
+  if (e == cudaSuccess) done[dev][key].store(true, std::memory_order_release);
+  return e;
+}
+
+int check_forward_args(const pw_moe_shape* shape, const void* hidden, const int32_t* topk_ids,
+                       const float* topk_weights, const pw_page_table* table, float* out,
+                       LayerArgs* a, bool* empty) {
+  *empty = false;
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  const pw_moe_shape& s = *shape;
+  if (table == nullptr) return fail(PW_ERR_INVALID_ARG, "table is NULL");
+  if (table->num_blocks != 2 * s.E)
+    return fail(PW_ERR_SHAPE, "page table has %d blocks, shape needs 2E = %d", table->num_blocks,
+                2 * s.E);
+  if (s.T == 0) {
+    *empty = true;
+    return PW_OK;
+  }
+  if (!hidden || !topk_ids || !topk_weights || !out)
+    return fail(PW_ERR_INVALID_ARG, "hidden, topk_ids, topk_weights and out must be non-NULL");
+  if (!aligned(hidden, 16) || !aligned(out, 16))
+    return fail(PW_ERR_INVALID_ARG, "hidden and out must be 16-byte aligned");
+  if (!aligned(topk_ids, 4) || !aligned(topk_weights, 4))
+    return fail(PW_ERR_INVALID_ARG, "topk_ids and topk_weights must be 4-byte aligned");
+  if ((rc = check_device())) return rc;
+  int dev = 0;
+  if ((rc = current_device(&dev))) return rc;
+  if (dev != table->device)
+    return fail(PW_ERR_INVALID_ARG, "current device %d is not the page table's device %d", dev,
+                table->device);
+  a->T = s.T;
+  a->H = s.H;
+  a->I = s.I;
+  a->E = s.E;
+  a->k = s.k;
+  a->hidden = static_cast<const uint16_t*>(hidden);
+  a->topk_ids = topk_ids;
+  a->topk_weights = topk_weights;
+  a->table = table->d_entries;
+  a->out = out;
+  a->status = table->d_status;
+  a->stats_counts = table->stats_counts;
+  a->stats_mass = table->stats_mass;
+  return PW_OK;
+}
 
 }  // namespace pw
 
@@ -398,6 +458,19 @@ int pw_moe_forward_path(const pw_moe_shape* shape, const void* hidden, const int
                         cudaStream_t stream) {
   return pw::forward_impl(shape, hidden, topk_ids, topk_weights, table, out, workspace,
                           workspace_bytes, path, stream);
+}
+
+int pw_debug_bounded_wait(pw_page_table* table, int32_t which, int32_t polls,
+                          cudaStream_t stream) {
+  if (table == nullptr) return fail(PW_ERR_INVALID_ARG, "table is NULL");
+  if (which != 0 && which != 1) return fail(PW_ERR_INVALID_ARG, "which must be 0 or 1");
+  if (polls < 1 || polls > (1 << 20)) return fail(PW_ERR_INVALID_ARG, "polls outside 1..2^20");
+  int rc = pw::check_device();
+  if (rc) return rc;
+  const cudaError_t e =
+      which == 0 ? pw::launch_wait_check_decode(table->d_status, static_cast<uint32_t>(polls), stream)
+                 : pw::launch_wait_check_mbar(table->d_status, static_cast<uint32_t>(polls), stream);
+  return e == cudaSuccess ? PW_OK : cuda_fail(e, "bounded-wait check launch");
 }
 
 int32_t pw_prefill_min_pairs(const pw_moe_shape* shape) {

@@ -67,7 +67,7 @@ cudaError_t launch_pack_bitplanes(const uint8_t* codes, int N, int K, uint32_t* 
                                   cudaStream_t s) {
   const long long n_words = static_cast<long long>(N) * (K / 32);
   if (n_words == 0) return cudaSuccess;
-  pack_bitplanes_kernel<<<grid_for(n_words, 8, 152 * 64), 256, 0, s>>>(codes, N, K, planes);
+  pack_bitplanes_kernel<<<grid_for(n_words, 8, 64 * sm_count()), 256, 0, s>>>(codes, N, K, planes);
   return cudaGetLastError();
 }
 
@@ -75,7 +75,7 @@ cudaError_t launch_unpack_top(const uint32_t* planes, int N, int K, int b, uint8
                               cudaStream_t s) {
   const long long total = static_cast<long long>(N) * K;
   if (total == 0) return cudaSuccess;
-  unpack_top_kernel<<<grid_for(total, 256, 152 * 64), 256, 0, s>>>(planes, N, K, b, idx);
+  unpack_top_kernel<<<grid_for(total, 256, 64 * sm_count()), 256, 0, s>>>(planes, N, K, b, idx);
   return cudaGetLastError();
 }
 

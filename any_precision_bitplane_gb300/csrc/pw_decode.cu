@@ -417,9 +417,9 @@ __device__ __forceinline__ int load_relaxed(const int* p) {
 // Gives up after kReadySpinLimit polls and latches PW_ERR_TIMEOUT (the tile
 // then runs on whatever h holds).
 __device__ __forceinline__ void wait_gate_up(const int* done, int seen, int need,
-                                             int32_t* status) {
+                                             int32_t* status, uint32_t limit = kReadySpinLimit) {
   for (uint32_t i = 0; seen < need; ++i) {
-    if (i == kReadySpinLimit) {
+    if (i == limit) {
       latch_status(status, PW_ERR_TIMEOUT);
       break;
     }
@@ -427,6 +427,17 @@ __device__ __forceinline__ void wait_gate_up(const int* done, int seen, int need
     seen = load_relaxed(done);
   }
   __threadfence();
+}
+
+// A counter that nothing ever increments: the bounded-wait check below waits
+// on it so that the wait must run out.
+__device__ int g_never_released = 0;
+
+// Failure-detection check: the down kernel's wait for an expert's gate_up
+// tiles, run by one thread on a counter nobody releases, with `limit` polls.
+// It must give up, latch PW_ERR_TIMEOUT and return.
+__global__ void wait_check_kernel(int32_t* status, uint32_t limit) {
+  if (threadIdx.x == 0) wait_gate_up(&g_never_released, load_relaxed(&g_never_released), 1, status, limit);
 }
 
 // ---------------------------------------------------------------- gate_up
@@ -976,6 +987,11 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
 
 }  // namespace
 
+cudaError_t launch_wait_check_decode(int32_t* status, uint32_t polls, cudaStream_t s) {
+  wait_check_kernel<<<1, 32, 0, s>>>(status, polls);
+  return cudaGetLastError();
+}
+
 int decode_max_pairs() { return kMaxPairs; }
 int decode_max_experts() { return kMaxExperts; }
 
@@ -1000,17 +1016,6 @@ WsSizes ws_sizes(const pw_moe_shape& s) {
   z.arrive = round256(4 * static_cast<size_t>(s.H / 32));
   z.gu_done = round256(4 * static_cast<size_t>(s.E));
   return z;
-}
-
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
 }
 
 // A launch that may start while the previous kernel on the stream finishes
@@ -1051,18 +1056,22 @@ size_t decode_workspace_bytes(const pw_moe_shape& s, bool hybrid) {
   return base + ((hybrid && hybrid_possible(s)) ? heavy_scratch_bytes(s) : 0);
 }
 
+namespace {
+// The >48 KB shared-memory opt-in of the decode kernels, set once per device.
+cudaError_t configure_decode() {
+  cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kSmemBytes));
+}
+}  // namespace
+
 cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, bool hybrid) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e0 = setup_once(kSetupDecode, configure_decode);
+  if (e0 != cudaSuccess) return e0;
+  const int sms = sm_count();
   const int n_pairs = a.T * a.k;
   if (n_pairs == 0) return cudaSuccess;
   pw_moe_shape shape{a.T, a.H, a.I, a.E, a.k};
@@ -1083,7 +1092,7 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
   w.heavy_min = heavy ? kHeavyMinTokens : 0;
   // grids: at most one tile per resident CTA (2 per SM)
   const int slots = a.E < n_pairs ? a.E : n_pairs;
-  const int resident = 2 * sm_count();
+  const int resident = 2 * sms;
   const int gu_tiles = slots * (a.I / kPairsPerTile);
   const int dn_tiles = slots * ((a.H + kDownRows - 1) / kDownRows);
 
@@ -1096,7 +1105,7 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
   }
   const long long n4 = static_cast<long long>(a.T) * a.H / 4;
   const long long conv = (n4 + kPrepThreads - 1) / kPrepThreads;
-  const int prep_grid = 1 + static_cast<int>(conv < 4 * 152 ? conv : 4 * 152);
+  const int prep_grid = 1 + static_cast<int>(conv < 4 * sms ? conv : 4 * sms);
   // Small calls (the down grid leaves SM slots free) launch the prep early
   // and let the down grid release it: it becomes resident while the previous
   // call's down grid runs and starts the moment that grid completes.

@@ -22,6 +22,30 @@ int fail(int code, const char* fmt, ...);
 int cuda_fail(cudaError_t err, const char* what);
 void clear_error();
 
+// ---- per-device state (host) -------------------------------------------------
+// Everything cached on the host is keyed by the device ordinal, so calls on
+// several devices of one process (each with that device current) each get
+// their own set-up and SM count.  All of it is safe to call from several
+// host threads.
+constexpr int kMaxDevices = 64;
+enum SetupKey { kSetupDecode = 0, kSetupGemm = 1, kSetupKeys = 2 };
+// Ordinal of the current device (PW_OK), or an error status with a message.
+int current_device(int* dev);
+// SM count of the current device (at least 1).
+int sm_count();
+// Runs `fn` (kernel attribute set-up) once per (key, current device); later
+// calls return cudaSuccess without running it.  A failure is not cached.
+cudaError_t setup_once(SetupKey key, cudaError_t (*fn)());
+
+// Checks shared by the forward entry points (pw_moe_forward[_path] and
+// pw_moe_forward_noalloc): shape, table, pointers and alignment, and that the
+// current device is an sm_103 device and the table's device.  Fills *a; sets
+// *empty when the call has no tokens (nothing to launch).
+struct LayerArgs;
+int check_forward_args(const pw_moe_shape* shape, const void* hidden, const int32_t* topk_ids,
+                       const float* topk_weights, const pw_page_table* table, float* out,
+                       LayerArgs* a, bool* empty);
+
 // ---- device helpers ----------------------------------------------------------
 __device__ __forceinline__ void latch_status(int32_t* status, int32_t code) {
   if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
@@ -106,5 +130,10 @@ bool prefill_shape_ok(const pw_moe_shape& s);  // H % 128 == 0, I % 64 == 0, E <
 size_t heavy_scratch_bytes(const pw_moe_shape& s);
 cudaError_t launch_heavy(const LayerArgs& a, const int32_t* offsets, const int32_t* perm, float* y,
                          void* scratch, int min_tokens, cudaStream_t s);
+
+// Failure-detection checks (pw_debug_bounded_wait): one bounded device wait
+// of the forward kernels run against something never released.
+cudaError_t launch_wait_check_decode(int32_t* status, uint32_t polls, cudaStream_t s);
+cudaError_t launch_wait_check_mbar(int32_t* status, uint32_t polls, cudaStream_t s);
 
 }  // namespace pw

@@ -23,7 +23,6 @@ namespace pw {
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
@@ -54,23 +53,14 @@ extern "C" int pw_moe_forward_noalloc(const pw_moe_shape* shape, const void* hid
                                       const pw_page_table* table, float* out,
                                       cudaStream_t stream) {
   using pw::fail;
-  if (shape == nullptr) return fail(PW_ERR_INVALID_ARG, "shape is NULL");
+  // the same argument checks as pw_moe_forward, including that the current
+  // device is the table's device (so the scratch address below is that
+  // device's copy of the array)
+  pw::LayerArgs a;
+  bool empty = false;
+  int rc = pw::check_forward_args(shape, hidden, topk_ids, topk_weights, table, out, &a, &empty);
+  if (rc || empty) return rc;
   const pw_moe_shape& s = *shape;
-  if (s.T < 0 || s.H <= 0 || s.I <= 0 || s.E <= 0 || s.k <= 0)
-    return fail(PW_ERR_INVALID_ARG, "shape has a non-positive size (T=%d H=%d I=%d E=%d k=%d)",
-                s.T, s.H, s.I, s.E, s.k);
-  if (s.H % 32 || s.I % 32)
-    return fail(PW_ERR_SHAPE, "H (%d) and I (%d) must be multiples of 32", s.H, s.I);
-  if (s.k > s.E) return fail(PW_ERR_SHAPE, "k (%d) > E (%d)", s.k, s.E);
-  if (table == nullptr) return fail(PW_ERR_INVALID_ARG, "table is NULL");
-  if (table->num_blocks != 2 * s.E)
-    return fail(PW_ERR_SHAPE, "page table has %d blocks, shape needs 2E = %d", table->num_blocks,
-                2 * s.E);
-  if (s.T == 0) return PW_OK;
-  if (!hidden || !topk_ids || !topk_weights || !out)
-    return fail(PW_ERR_INVALID_ARG, "hidden, topk_ids, topk_weights and out must be non-NULL");
-  if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(out)) % 16)
-    return fail(PW_ERR_INVALID_ARG, "hidden and out must be 16-byte aligned");
   const long long n_pairs = static_cast<long long>(s.T) * s.k;
   if (n_pairs > pw::decode_max_pairs() || s.E > pw::decode_max_experts())
     return fail(PW_ERR_SHAPE, "decode path limits: T*k <= %d, E <= %d", pw::decode_max_pairs(),
@@ -82,33 +72,10 @@ extern "C" int pw_moe_forward_noalloc(const pw_moe_shape* shape, const void* hid
                 "pw_moe_forward_noalloc holds %zu bytes (use pw_moe_forward with a workspace)",
                 need, pw::kStaticScratchBytes);
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return pw::cuda_fail(e, "cudaGetDevice");
-  int major = 0, minor = 0;
-  if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
-      (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
-    return pw::cuda_fail(e, "cudaDeviceGetAttribute");
-  if (major != 10 || minor != 3)
-    return fail(PW_ERR_UNSUPPORTED_DEVICE, "device %d is sm_%d%d; libpw is built for sm_103a", dev,
-                major, minor);
+  if ((rc = pw::current_device(&dev))) return rc;
   void* scratch = nullptr;
-  int rc = pw::static_scratch_address(dev, &scratch);
-  if (rc) return rc;
-  pw::LayerArgs a;
-  a.T = s.T;
-  a.H = s.H;
-  a.I = s.I;
-  a.E = s.E;
-  a.k = s.k;
-  a.hidden = static_cast<const uint16_t*>(hidden);
-  a.topk_ids = topk_ids;
-  a.topk_weights = topk_weights;
-  a.table = table->d_entries;
-  a.out = out;
-  a.status = table->d_status;
-  a.stats_counts = table->stats_counts;
-  a.stats_mass = table->stats_mass;
-  e = pw::launch_decode(a, scratch, stream, false);
+  if ((rc = pw::static_scratch_address(dev, &scratch))) return rc;
+  cudaError_t e = pw::launch_decode(a, scratch, stream, false);
   if (e != cudaSuccess) return pw::cuda_fail(e, "forward launch");
   return PW_OK;
 }

@@ -14,7 +14,7 @@
 //              over one half of K, epilogue y[pair] or y2[pair] (fp32)
 //   combine    out[t] = sum_j w_tj * (y + y2)[t*k + j], j order (one pass)
 //
-// GEMM kernel: one CTA per SM, persistent, 23 warps in five roles.
+// GEMM kernel: one CTA per SM, persistent, 27 warps in five roles.
 //   warp 20     scheduler and token-operand producer: takes tile ids from a
 //               global counter (SMs that draw cheap tiles take more of them),
 //               publishes each through a 4-deep ring in shared memory, and
@@ -171,14 +171,29 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // Bounded wait: false if the CTA is aborting or the limit ran out (which
 // latches the timeout and starts the abort).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int32_t* status) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+                                          int32_t* status, uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try(bar, parity)) return true;
     if (*abort) return false;
   }
   *abort = 1;
   latch_status(status, PW_ERR_TIMEOUT);
   return false;
+}
+
+// Failure-detection check: the tensor-core kernels' bounded mbarrier wait,
+// run by one thread on a barrier that expects one arrival that never comes
+// (phase 0 never completes), with `limit` polls.  It must give up, latch
+// PW_ERR_TIMEOUT, raise the abort flag and return.
+__global__ void mbar_wait_check_kernel(int32_t* status, uint32_t limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(smem_u32(&bar), 0, &abort_flag, status, limit);
+  }
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -976,18 +991,23 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int cols) {
   return r == CUDA_SUCCESS;
 }
 
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
+// The >48 KB shared-memory opt-in of both GEMM instantiations, set once per
+// device.
+cudaError_t configure_gemm() {
+  cudaError_t e = cudaFuncSetAttribute(dq_gemm_kernel<kGateUp>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(dq_gemm_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kSmemBytes));
 }
 
 }  // namespace
+
+cudaError_t launch_wait_check_mbar(int32_t* status, uint32_t polls, cudaStream_t s) {
+  mbar_wait_check_kernel<<<1, 32, 0, s>>>(status, polls);
+  return cudaGetLastError();
+}
 
 size_t heavy_scratch_bytes(const pw_moe_shape& s) {
   const size_t P = static_cast<size_t>(s.T) * s.k;
@@ -1000,17 +1020,9 @@ size_t heavy_scratch_bytes(const pw_moe_shape& s) {
 // combine.
 cudaError_t launch_heavy(const LayerArgs& la, const int32_t* offsets, const int32_t* perm, float* y,
                          void* scratch, int min_tokens, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(dq_gemm_kernel<kGateUp>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(dq_gemm_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e0 = setup_once(kSetupGemm, configure_gemm);
+  if (e0 != cudaSuccess) return e0;
+  const int sms = sm_count();
   const int n_pairs = la.T * la.k;
   const size_t P = static_cast<size_t>(n_pairs);
   char* p = static_cast<char*>(scratch);
@@ -1020,7 +1032,7 @@ cudaError_t launch_heavy(const LayerArgs& la, const int32_t* offsets, const int3
   p += round256(2 * P * la.H);
   __half* h = reinterpret_cast<__half*>(p);
   const long long gwork = static_cast<long long>(n_pairs) * (la.H / 8);
-  const int gblocks = static_cast<int>(std::min<long long>((gwork + 255) / 256, 152LL * 32));
+  const int gblocks = static_cast<int>(std::min<long long>((gwork + 255) / 256, 32LL * sms));
   gather_kernel<<<gblocks, 256, 0, stream>>>(la.hidden, perm, offsets, la.E, la.k, la.H, n_pairs, xg,
                                              counters);
   cudaError_t e = cudaGetLastError();
@@ -1043,7 +1055,7 @@ cudaError_t launch_heavy(const LayerArgs& la, const int32_t* offsets, const int3
   g.ksplit = 1;   // the decode path's combine reads one y
   g.status = la.status;
   g.min_tokens = min_tokens;
-  const int grid = num_sms();
+  const int grid = sms;
   const BitConsts bc = make_bit_consts();
   g.tile_counter = counters;
   dq_gemm_kernel<kGateUp><<<grid, kThreads, kSmemBytes, stream>>>(g, map_x, bc);
@@ -1066,17 +1078,9 @@ bool prefill_shape_ok(const pw_moe_shape& s) {
 int prefill_min_pairs(const pw_moe_shape& s) { return prefill_shape_ok(s) ? 1024 : INT_MAX; }
 
 cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(dq_gemm_kernel<kGateUp>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(dq_gemm_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e0 = setup_once(kSetupGemm, configure_gemm);
+  if (e0 != cudaSuccess) return e0;
+  const int sms = sm_count();
   pw_moe_shape s{la.T, la.H, la.I, la.E, la.k};
   const int n_pairs = la.T * la.k;
   if (n_pairs == 0) return cudaSuccess;
@@ -1086,7 +1090,7 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if ((e = launch_routing_stats(la, stream)) != cudaSuccess) return e;
   const long long gwork = static_cast<long long>(n_pairs) * (la.H / 8);
-  const int gblocks = static_cast<int>(std::min<long long>((gwork + 255) / 256, 152LL * 32));
+  const int gblocks = static_cast<int>(std::min<long long>((gwork + 255) / 256, 32LL * sms));
   gather_kernel<<<gblocks, 256, 0, stream>>>(la.hidden, w.perm, w.offsets, la.E, la.k, la.H,
                                              n_pairs, w.xg, w.counters);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1109,7 +1113,7 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   g.ksplit = 1;
   g.status = la.status;
   g.min_tokens = 1;
-  const int grid = num_sms();
+  const int grid = sms;
   const BitConsts bc = make_bit_consts();
   g.tile_counter = w.counters;
   if ((e = record_timing(g_timing.before, stream)) != cudaSuccess) return e;
@@ -1125,7 +1129,7 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   dq_gemm_kernel<kDown><<<grid, kThreads, kSmemBytes, stream>>>(g, map_h, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long cwork = static_cast<long long>(la.T) * (la.H / 4);
-  const int cblocks = static_cast<int>(std::min<long long>((cwork + 255) / 256, 152LL * 32));
+  const int cblocks = static_cast<int>(std::min<long long>((cwork + 255) / 256, 32LL * sms));
   combine_kernel<<<cblocks, 256, 0, stream>>>(w.y, g.ksplit == 2 ? w.y2 : nullptr, la.topk_ids,
                                               la.topk_weights, la.T, la.k, la.E, la.H, la.out);
   return cudaGetLastError();

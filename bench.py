@@ -27,7 +27,14 @@ import sys
 import threading
 import time
 
-import numpy as np
+# The CPU baseline's BLAS (NumPy's fp64 matmuls inside the oracle) runs on
+# every host core; the thread count is fixed here, before NumPy loads, so
+# that the reported core count is the one actually used.
+HOST_CORES = os.cpu_count() or 1
+for _var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_var, str(HOST_CORES))
+
+import numpy as np  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -331,6 +338,24 @@ def _oracle_setup(name, T):
     return cfg, tok, ids, w.astype(np.float32), (lambda e, m: encoded[(e, m)])
 
 
+def blas_threads():
+    """Threads NumPy's BLAS uses: read back through threadpoolctl where it is
+    installed, else the thread-count variable set before NumPy loaded."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [int(i["num_threads"]) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n), "threadpoolctl"
+    except Exception:
+        pass
+    return int(os.environ.get("OPENBLAS_NUM_THREADS", "1")), "OPENBLAS_NUM_THREADS"
+
+
+def host_cores_entry():
+    n, how = blas_threads()
+    return {"cores": n, "cpu_count": HOST_CORES, "blas_threads": n, "blas_threads_from": how}
+
+
 def cpu_baseline(name, T, budget_s=20.0):
     """The oracle as it stands, on host cores, over a bounded sample: whole
     decode batches (stops after ~budget_s or 3 batches)."""
@@ -344,10 +369,12 @@ def cpu_baseline(name, T, budget_s=20.0):
         if time.perf_counter() - t0 > budget_s or calls >= 3:
             break
     dt = time.perf_counter() - t0
-    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "%d full forward(s) of the T=%d batch: fp64 NumPy in one process "
-                      "(top-q unpack + LUT dequant of every routed block, matmuls, combine; "
-                      "blocks encoded before timing)" % (calls, T)}
+    entry = {"value": done / dt, "unit": "tokens/s", "kind": "oracle",
+             "sample": "%d full forward(s) of the T=%d batch: fp64 NumPy in one process "
+                       "(top-q unpack + LUT dequant of every routed block, matmuls on the "
+                       "BLAS threads, combine; blocks encoded before timing)" % (calls, T)}
+    entry.update(host_cores_entry())
+    return entry
 
 
 def hidden_bytes(cfg, T):
@@ -634,9 +661,10 @@ def reference(args):
         "data": "synthetic",
         "config": {"workload": "%s: H=%d I=%d E=%d top-%d, T=%d tokens per step" %
                                (cfg.name, cfg.H, cfg.I, cfg.E, cfg.k, args.T)},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "each step: one routed (token, expert) pair of the batch "
-                                   "through the oracle, i.e. 1/%d of a token" % k},
+        "cpu_baseline": dict({"value": value, "unit": "tokens/s", "kind": "oracle",
+                              "sample": "each step: one routed (token, expert) pair of the "
+                                        "batch through the oracle, i.e. 1/%d of a token" % k},
+                             **host_cores_entry()),
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)

@@ -325,6 +325,24 @@ int32_t pw_prefill_min_pairs(const pw_moe_shape* shape);
  * and not thread-safe.  Errors: PW_ERR_INVALID_ARG (exactly one is NULL). */
 int pw_set_timing_events(cudaEvent_t before, cudaEvent_t after);
 
+/* ---- failure-detection check -------------------------------------------------
+ * No counterpart on the PagedWeight pages.  Every device-side wait of the
+ * forward kernels is bounded so that a wait that can never end (a producer
+ * that stopped, a barrier nobody arrives at) costs a status code, not a hung
+ * GPU.  This entry point proves that on the device without starving a real
+ * forward call: it runs one of those waits, the same device code with a
+ * caller-chosen limit, against something that is never released:
+ *   which 0: the decode down kernel's wait for an expert's gate_up tiles,
+ *            on a counter nothing increments (each poll sleeps ~128 ns);
+ *   which 1: the tensor-core kernels' mbarrier wait, on a barrier whose
+ *            phase never completes.
+ * After `polls` polls the wait gives up, latches PW_ERR_TIMEOUT in the table's
+ * status word (read with pw_page_table_status) and the kernel returns; the
+ * context stays usable.  Errors: PW_ERR_INVALID_ARG (NULL table, which not 0
+ * or 1, polls outside 1..2^20), PW_ERR_UNSUPPORTED_DEVICE, PW_ERR_CUDA. */
+int pw_debug_bounded_wait(pw_page_table* table, int32_t which, int32_t polls,
+                          cudaStream_t stream);
+
 /* ---- the fused layer without a workspace ------------------------------------
  * The PagedWeight pages have no counterpart to this entry point; it is a
  * service for callers that cannot allocate device memory: a plugin whose

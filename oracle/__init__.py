@@ -30,5 +30,7 @@ Pinning status (what each function is checked against in tests/):
   moe_forward                  -- explicit triple-loop brute force on tiny
                                   inputs (computed from the codes, not the
                                   planes); one-hot and constant-LUT closed forms.
+  rel_l2                       -- closed-form values worked by hand from the
+                                  metric's definition (tests/golden/).
 """
 from . import apl, moe  # noqa: F401

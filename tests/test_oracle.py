@@ -231,6 +231,35 @@ def test_silu_textbook_values():
         assert math.isclose(float(moe.silu(np.float64(g))), v, rel_tol=1e-15, abs_tol=1e-300)
 
 
+# ---------------------------------------------------------------- parity metric
+
+def test_rel_l2_closed_forms():
+    # the metric every GPU parity test uses, pinned by values worked by hand
+    # from its definition (tests/golden/rel_l2_closed_forms.txt)
+    with open(os.path.join(GOLDEN, "rel_l2_closed_forms.txt")) as f:
+        lines = [ln for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(lines) >= 8
+    for ln in lines:
+        got, ref, want = (part.split() for part in ln.split("|"))
+        got = np.array([float(v) for v in got])
+        ref = np.array([float(v) for v in ref])
+        assert math.isclose(moe.rel_l2(got, ref), float(want[0]), rel_tol=1e-12, abs_tol=1e-15), ln
+
+
+def test_rel_l2_scales_and_shapes():
+    # scale invariance, 2-D tensors, and eps * ref giving exactly eps
+    rng = np.random.default_rng(9)
+    ref = rng.standard_normal((7, 5))
+    for eps in (1e-6, 2e-3, 0.5):
+        assert math.isclose(moe.rel_l2(ref * (1 + eps), ref), eps, rel_tol=1e-9)
+        assert math.isclose(moe.rel_l2(1e8 * ref * (1 + eps), 1e8 * ref), eps, rel_tol=1e-9)
+    # the error is pooled over the whole tensor, not averaged per row
+    got = ref.copy()
+    got[3] += 1.0
+    want = math.sqrt(5.0) / math.sqrt(float((ref ** 2).sum()))
+    assert math.isclose(moe.rel_l2(got, ref), want, rel_tol=1e-12)
+
+
 # ---------------------------------------------------------------- full layer
 
 def _layer_blocks(layer):
@@ -278,6 +307,7 @@ def test_moe_forward_matches_brute_force():
     w32 = w.astype(np.float32)
     got = moe.moe_forward(tok.hidden_bf16, ids, w32, _layer_blocks(layer), cfg.E)
     want = _brute_force_layer(layer, tok.hidden_bf16, ids, w32)
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-14)
     assert moe.rel_l2(got, want) < 1e-12
 
 
