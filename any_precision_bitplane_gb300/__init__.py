@@ -24,6 +24,7 @@ PW_ERR_BAD_EXPERT_ID = 6
 PW_ERR_CUDA = 7
 PW_ERR_TIMEOUT = 8
 PW_ERR_UNSUPPORTED_DEVICE = 9
+PW_ERR_RANGE = 10
 
 PW_PAGE_GPU = 0
 PW_PAGE_CPU = 1

@@ -39,13 +39,30 @@
 // streams its word columns through a 3-stage cp.async ring: per column, one
 // word of each of the top q planes per row (a word column of consecutive
 // rows is contiguous, so each copy is part of a 128-byte line) plus the 32
-// matching activations of up to 4 tokens.  A lane turns its q words into 32
-// index bytes with a byte transpose and an 8x8 bit-matrix transpose and
-// looks each index up in its row's LUT, held in a lane-private
-// shared-memory column (every lookup of lane L hits bank L); a byte permute
-// of the index byte forms the offset.  Products accumulate as packed fp32
-// pairs.  q = 8 blocks stream one row per lane so that their LUTs fit.
+// matching activations of up to 4 tokens.  A lane turns its q plane words
+// into indices with a register-index / bit-position transpose (swap stages
+// of shifts and bit selects, no byte shuffles); the indices come out in a
+// fixed permuted column order, and the activations are stored in that same
+// order, so every product still pairs a weight with its own column.  Two
+// lookup forms, by bitwidth:
+//   q = 3, 4  nibble indices; one byte of them is a pair of columns, looked
+//             up in a pair table of the row (2^2q entries, each the fp16
+//             pair {LUT[a], LUT[b]}) with one byte permute and one shared
+//             load per two weights; products are packed fp16 pairs against
+//             fp16 activations, summed in fp16 over the 16 pairs of a word
+//             column and then added to fp32 accumulators with the column
+//             group's power-of-two scale (activations are stored per group
+//             of 32 as x * 2^-e with max |x * 2^-e| in [1, 2), so no fp16
+//             value overflows and the fp16 partial sums keep their relative
+//             precision);
+//   q = 5, 6, 8  byte indices, one lookup per weight in the row's fp32 LUT;
+//             products accumulate as packed fp32 pairs against fp32
+//             activations.
+// Every lookup of lane L hits bank L (the tables are lane-interleaved).
+// q = 4 and q = 8 blocks stream one row per lane so that their tables fit.
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "pw_bits.cuh"
 #include "pw_internal.cuh"
@@ -72,12 +89,13 @@ constexpr int kStagePlaneBytes = 12 * 128;
 constexpr int kStageBytes = kStagePlaneBytes + kTG * 128;
 
 // Shared memory (bytes).  LUT region first.  Two layouts:
-//   paired  (q <= 6, two row slots): entry v of slot g for lane L at
-//           v*256 + g*128 + L*4, so one byte permute of the index byte forms
-//           the offset;
-//   compact (q = 8, one row slot):   entry v for lane L at v*128 + L*4 (the
-//           permute gives v*256 + L*8, halved by one shift).
-// Either way a lane's lookups always hit bank L.
+//   paired  (two row slots): entry v of slot g for lane L at v*256 + g*128
+//           + L*4, so one byte permute of the index byte forms the offset;
+//   compact (one row slot):  entry v for lane L at v*128 + L*4 (the permute
+//           gives v*256 + L*8, halved by one shift).
+// Either way a lane's lookups always hit bank L.  An entry is an fp32 weight
+// (q = 5, 6, 8) or an fp16 pair of weights indexed by two nibble indices
+// (q = 3 paired, q = 4 compact).
 constexpr int kLutBytes = 32768;
 constexpr int kRingBytes = kWarps * kStages * kStageBytes;
 constexpr int kRedBytes = kWarps * kTG * 2 * 32 * 4;
@@ -117,15 +135,27 @@ struct SlotInfo {
   int32_t ne;       // pairs routed to e
   int32_t q;        // committed bitwidth of the block
   int32_t err;      // 0 if the tiles can run, else the status to latch
-  int32_t pad;
+  int32_t q_other;  // bitwidth of the expert's other block (gate_up: the down
+                    // block, whose form decides how h is stored)
   const uint32_t* planes;
   const uint16_t* lut;
 };
 
 // Workspace of one decode call.
+// Activations come in two forms, matching the two lookup forms (the column
+// order inside each group of 32 is the one the index form produces):
+//   fp32 form  float [rows][K], column c of a group at byte_form_position(c);
+//   fp16 form  one 80-byte record per (row, group of 32 columns): 32 fp16
+//              values x * 2^-e at nibble_form_position(c), then the float
+//              2^e at byte 64 (e puts the group's largest |x * 2^-e| in
+//              [1, 2)), then padding.
+constexpr int kRecBytes = 80;
+
 struct DecodeWs {
-  float* x32;      // [T][H]   hidden states widened to fp32
-  float* h;        // [P][I]   SiLU(g) * u, by grouped pair position
+  float* xs;       // [T][H]   hidden states, fp32 form
+  char* xp;        // [T][H/32] records: hidden states, fp16 form
+  float* hs;       // [P][I]   SiLU(g) * u by grouped pair position, fp32 form
+  char* hp;        // [P][I/32] records: the same in fp16 form (down blocks at q <= 4)
   float* y;        // [P][H]   expert output, by pair id
   int* offsets;    // [E+1]    expert e owns grouped positions offsets[e] .. offsets[e+1]
   int* perm;       // [P]      grouped position -> pair id
@@ -168,15 +198,6 @@ __device__ __forceinline__ int seg_base(const PassRows<R>& pr, int g, int seg) {
   return g ? b : a;
 }
 
-template <int NT>
-__device__ __forceinline__ const float* pick(const float* const (&xs)[NT], int tk) {
-  const float* p = xs[0];
-#pragma unroll
-  for (int i = 1; i < NT; ++i)
-    if (tk == i) p = xs[i];
-  return p;
-}
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -195,11 +216,32 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// LUT rows of one pass into shared memory as fp32 (layouts above), in two
-// steps so that the round trip overlaps other set-up work: lut_fetch issues
-// every global load of the thread (up to four 16-byte pieces of 8 fp16
-// entries) into registers, lut_store converts and stores them.  A warp's
-// stores hit 32 banks.
+// Lookup form of a block at bitwidth Q: pair tables with nibble indices for
+// Q <= 4 (fp16 products), fp32 tables with byte indices otherwise.
+template <int Q>
+struct Form {
+  static constexpr bool kPair = Q <= 4;
+  // bytes of one token's activations in a ring stage (a record, or 32 floats)
+  static constexpr int kXBytes = kPair ? kRecBytes : 128;
+  static constexpr int kXChunks = kXBytes / 16;
+};
+
+// Power-of-two group scale: e with m * 2^-e in [1, 2) for the group's largest
+// magnitude m (clamped so that 2^e and 2^-e are normal floats).
+__device__ __forceinline__ int group_exponent(float m) {
+  const int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+  return min(max(e, -126), 126);
+}
+
+__device__ __forceinline__ float exp2i(int e) {
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
+// fp32 tables (Q = 5, 6, 8): the LUT rows of one pass into shared memory
+// (layouts above), in two steps so that the round trip overlaps other set-up
+// work: lut_fetch issues every global load of the thread (up to four 16-byte
+// pieces of 8 fp16 entries) into registers, lut_store converts and stores
+// them.  A warp's stores hit 32 banks.
 template <int Q, int R>
 struct LutPieces {
   static constexpr int kEnt = 1 << Q;
@@ -247,24 +289,115 @@ __device__ __forceinline__ void lut_store(const LutPieces<Q, R>& lp) {
   }
 }
 
+// Pair tables (Q = 3, 4): entry v = a + 16 b of a row holds the fp16 pair
+// {LUT[a], LUT[b]} (low half a), looked up by one byte of nibble indices.
+// kTPR threads build each row's table; thread c of a row fetches the row's
+// whole LUT (2^Q fp16 values, one or two 16-byte loads) and writes the
+// entries whose high nibble b is in its share.  Only pairs of valid indices
+// are written (Q = 3: a, b < 8).
+template <int Q, int R>
+struct PairLutPieces {
+  static constexpr int kTPR = 8 / R;                 // threads per row (R*32 rows)
+  static constexpr int kBPT = (1 << Q) / kTPR;       // b values per thread
+  static constexpr int kWords = (1 << Q) / 2;        // u32 words of a row's LUT
+  uint32_t w[kWords];
+};
+
+template <int Q, int R>
+__device__ __forceinline__ void pair_lut_fetch(const uint16_t* lut, const PassRows<R>& pr,
+                                               PairLutPieces<Q, R>& lp) {
+  using L = PairLutPieces<Q, R>;
+  const int rho = threadIdx.x / L::kTPR;
+  const int g = rho >> 5, lane = rho & 31;
+  const int row = seg_base<R>(pr, g, lane >> 4) + (lane & 15);
+  const uint4* src = reinterpret_cast<const uint4*>(lut + static_cast<long long>(row) * (1 << Q));
+#pragma unroll
+  for (int v = 0; v < L::kWords / 4; ++v) {
+    const uint4 q4 = __ldg(src + v);
+    lp.w[4 * v] = q4.x;
+    lp.w[4 * v + 1] = q4.y;
+    lp.w[4 * v + 2] = q4.z;
+    lp.w[4 * v + 3] = q4.w;
+  }
+}
+
+// Largest LUT magnitude a pair-table block supports: 16 products of such a
+// value with activations below 2 in magnitude stay inside fp16's range.
+constexpr uint32_t kPairLutLimitBits = 0x6800u;   // fp16 2048
+
+template <int Q, int R, bool COMPACT>
+__device__ __forceinline__ void pair_lut_store(const PairLutPieces<Q, R>& lp, int32_t* status) {
+  using L = PairLutPieces<Q, R>;
+  const int rho = threadIdx.x / L::kTPR, c = threadIdx.x % L::kTPR;
+  const int g = rho >> 5, lane = rho & 31;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < L::kWords; ++i)
+    bad |= ((lp.w[i] & 0x7FFFu) >= kPairLutLimitBits) || (((lp.w[i] >> 16) & 0x7FFFu) >= kPairLutLimitBits);
+  if (bad) latch_status(status, PW_ERR_RANGE);
+  const uint32_t base = COMPACT ? static_cast<uint32_t>(lane * 4)
+                                : static_cast<uint32_t>(g * 128 + lane * 4);
+  constexpr uint32_t kStride = COMPACT ? 128u : 256u;
+#pragma unroll
+  for (int bi = 0; bi < L::kBPT; ++bi) {
+    const int b = c * L::kBPT + bi;
+    // the word holding LUT[b] (runtime index into the register array)
+    uint32_t y = lp.w[0];
+#pragma unroll
+    for (int i = 1; i < L::kWords; ++i)
+      if ((b >> 1) == i) y = lp.w[i];
+    const uint32_t hi_sel = (b & 1) ? 0x7600u : 0x5400u;   // high half = LUT[b]
+#pragma unroll
+    for (int a = 0; a < (1 << Q); ++a) {
+      const uint32_t sel = hi_sel | ((a & 1) ? 0x32u : 0x10u);   // low half = LUT[a]
+      const uint32_t v = static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 4);
+      *reinterpret_cast<uint32_t*>(g_dsmem + v * kStride + base) = __byte_perm(lp.w[a >> 1], y, sel);
+    }
+  }
+}
+
+// The LUT of one pass, in the form of bitwidth Q: issued first (fetch), then
+// stored once the first ring columns are on their way (store).
+template <int Q, int R>
+struct PassLut {
+  using Pieces = typename std::conditional<Form<Q>::kPair, PairLutPieces<Q, R>, LutPieces<Q, R>>::type;
+  Pieces p;
+};
+
+template <int Q, int R>
+__device__ __forceinline__ void pass_lut_fetch(const uint16_t* lut, const PassRows<R>& pr,
+                                               PassLut<Q, R>& pl) {
+  if constexpr (Form<Q>::kPair) pair_lut_fetch<Q, R>(lut, pr, pl.p);
+  else lut_fetch<Q, R>(lut, pr, pl.p);
+}
+
+template <int Q, int R, bool COMPACT>
+__device__ __forceinline__ void pass_lut_store(const PassLut<Q, R>& pl, int32_t* status) {
+  if constexpr (Form<Q>::kPair) pair_lut_store<Q, R, COMPACT>(pl.p, status);
+  else lut_store<Q, R, COMPACT>(pl.p);
+}
+
 // The copies one lane issues for every word column: chunk c (16 bytes) of
 // a stage is plane p = (c/8)/R, row slot g = (c/8)%R, 16-row segment
 // (c/4)%2 and quarter c%4; it lands at stage byte c*16.  Its source is
 // planes + src_off + kw*N; the word offsets are fixed for a pass, so they are
-// computed once.  Activation chunk lane (< NT*8): token lane/8, 8 floats.
+// computed once.  Activation chunk lane (< NT * kXChunks): token
+// lane / kXChunks, 16-byte piece lane % kXChunks of the token's activations
+// for the word column (32 floats, or one fp16 record).
 template <int Q, int R, int NT>
 struct CopyPlan {
   static constexpr int kChunks = (Q * R * 8 + 31) / 32;
   uint32_t src_off[kChunks];
-  const float* x_src;   // token row + part offset (column 0)
+  const char* x_src;    // token row + piece offset (word column 0)
   uint32_t x_bytes;     // 16, or 0 to zero-fill an absent token
 };
 
 template <int Q, int R, int NT>
 __device__ __forceinline__ CopyPlan<Q, R, NT> make_copy_plan(long long plane_stride,
                                                              const PassRows<R>& pr,
-                                                             const float* const (&xs)[NT],
+                                                             const char* const (&xs)[NT],
                                                              int nt, int lane) {
+  constexpr int XC = Form<Q>::kXChunks;
   CopyPlan<Q, R, NT> cp;
 #pragma unroll
   for (int i = 0; i < CopyPlan<Q, R, NT>::kChunks; ++i) {
@@ -275,62 +408,77 @@ __device__ __forceinline__ CopyPlan<Q, R, NT> make_copy_plan(long long plane_str
                         ? static_cast<uint32_t>(p * plane_stride + seg_base<R>(pr, g, seg) + part * 4)
                         : 0u;
   }
-  const int tk = lane >> 3, part = lane & 7;
-  const bool live = lane < NT * 8 && tk < nt;
-  cp.x_src = (live ? pick<NT>(xs, tk) : xs[0]) + part * 4;
+  const int tk = lane / XC, part = lane % XC;
+  const bool live = lane < NT * XC && tk < nt;
+  const char* base = xs[0];
+#pragma unroll
+  for (int i = 1; i < NT; ++i)
+    if (live && tk == i) base = xs[i];
+  cp.x_src = base + part * 16;
   cp.x_bytes = live ? 16u : 0u;
   return cp;
 }
 
 // Start the asynchronous copies of word column kw of every streamed row and
-// of the matching 32 activations of each token into one ring stage.
+// of the matching activations of each token into one ring stage.
 template <int Q, int R, int NT>
 __device__ __forceinline__ void issue_column(uint32_t stage, const uint32_t* planes, long long N,
                                              const CopyPlan<Q, R, NT>& cp, int kw, int lane) {
+  constexpr int XC = Form<Q>::kXChunks;
   const uint32_t col = static_cast<uint32_t>(kw * N);
 #pragma unroll
   for (int i = 0; i < CopyPlan<Q, R, NT>::kChunks; ++i) {
     const int c = i * 32 + lane;
     if (c < Q * R * 8) cp_async16(stage + c * 16, planes + (cp.src_off[i] + col), 16);
   }
-  if (lane < NT * 8)
-    cp_async16(stage + kStagePlaneBytes + lane * 16, cp.x_src + (cp.x_bytes ? kw * 32 : 0),
+  if (lane < NT * XC)
+    cp_async16(stage + kStagePlaneBytes + lane * 16,
+               cp.x_src + (cp.x_bytes ? static_cast<long long>(kw) * Form<Q>::kXBytes : 0),
                cp.x_bytes);
 }
 
-// One word column from a ring stage: rebuild the 32 indices of each row,
-// look them up, and accumulate against NT tokens (packed fp32 pairs).
+__device__ __forceinline__ uint4 lds128(uint32_t off) {
+  return *reinterpret_cast<const uint4*>(g_dsmem + off);
+}
+
+// One word column from a ring stage, fp32 tables (Q = 5, 6, 8): byte indices
+// of each row, one lookup per weight, packed fp32 products.  B[r] byte b is
+// column 8b + r, whose activation sits at position 4r + b: the float4 at 4r.
 template <int Q, int R, int NT, bool COMPACT>
-__device__ __forceinline__ void compute_column(uint32_t stage, int lane, const BitConsts& bc,
-                                               float2 (&acc)[R][NT]) {
-  uint32_t cur[R][Q];
-#pragma unroll
-  for (int p = 0; p < Q; ++p)
-#pragma unroll
-    for (int g = 0; g < R; ++g)
-      cur[g][p] = *reinterpret_cast<const uint32_t*>(g_dsmem + stage + (p * R + g) * 128 + lane * 4);
+__device__ __forceinline__ void compute_column_bytes(uint32_t stage, int lane, const BitConsts& bc,
+                                                     float2 (&acc)[R][NT]) {
   uint32_t ib[R][8];
 #pragma unroll
-  for (int g = 0; g < R; ++g) planes_to_index_bytes<Q>(cur[g], ib[g], bc);
-  const float* xa = reinterpret_cast<const float*>(g_dsmem + stage + kStagePlaneBytes);
+  for (int g = 0; g < R; ++g) {
+    uint32_t cur[Q];
+#pragma unroll
+    for (int p = 0; p < Q; ++p)
+      cur[p] = *reinterpret_cast<const uint32_t*>(g_dsmem + stage + (p * R + g) * 128 + lane * 4);
+    planes_to_bytes<Q>(cur, ib[g], bc);
+  }
+  const uint32_t xa = stage + kStagePlaneBytes;
   uint32_t lb[R];
 #pragma unroll
   for (int g = 0; g < R; ++g)
     lb[g] = COMPACT ? (static_cast<uint32_t>(lane) << 3)
                     : ((static_cast<uint32_t>(g) << 7) | (static_cast<uint32_t>(lane) << 2));
 #pragma unroll
-  for (int m = 0; m < 8; ++m) {
+  for (int r = 0; r < 8; ++r) {
     float4 xv[NT];
 #pragma unroll
-    for (int tk = 0; tk < NT; ++tk) xv[tk] = *reinterpret_cast<const float4*>(xa + tk * 32 + 4 * m);
+    for (int tk = 0; tk < NT; ++tk) {
+      const uint4 u = lds128(xa + tk * 128 + r * 16);
+      xv[tk] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                           __uint_as_float(u.w));
+    }
 #pragma unroll
     for (int g = 0; g < R; ++g) {
       float w[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t off = __byte_perm(ib[g][m], lb[g], 0x6504 | (j << 4));
+      for (int b = 0; b < 4; ++b) {
+        uint32_t off = __byte_perm(ib[g][r], lb[g], 0x6504 | (b << 4));
         if (COMPACT) off >>= 1;
-        w[j] = *reinterpret_cast<const float*>(g_dsmem + off);
+        w[b] = *reinterpret_cast<const float*>(g_dsmem + off);
       }
 #pragma unroll
       for (int tk = 0; tk < NT; ++tk) {
@@ -341,12 +489,77 @@ __device__ __forceinline__ void compute_column(uint32_t stage, int lane, const B
   }
 }
 
+// One word column from a ring stage, pair tables (Q = 3, 4): nibble indices
+// of each row; byte j of N[r] pairs columns 8j + r and 8j + 4 + r, whose
+// fp16 activations sit at positions 8r + 2j and 8r + 2j + 1: half2 j of the
+// 16 bytes at 16r of the token's record.  The fp16 products of the column's
+// 16 pairs are summed in a half2, which is then added to the fp32
+// accumulator with the group's scale 2^e.
+template <int Q, int R, int NT, bool COMPACT>
+__device__ __forceinline__ void compute_column_pairs(uint32_t stage, int lane, const BitConsts& bc,
+                                                     float2 (&acc)[R][NT]) {
+  uint32_t nb[R][4];
+#pragma unroll
+  for (int g = 0; g < R; ++g) {
+    uint32_t cur[Q];
+#pragma unroll
+    for (int p = 0; p < Q; ++p)
+      cur[p] = *reinterpret_cast<const uint32_t*>(g_dsmem + stage + (p * R + g) * 128 + lane * 4);
+    planes_to_nibbles<Q>(cur, nb[g], bc);
+  }
+  const uint32_t xa = stage + kStagePlaneBytes;
+  uint32_t lb[R];
+#pragma unroll
+  for (int g = 0; g < R; ++g)
+    lb[g] = COMPACT ? (static_cast<uint32_t>(lane) << 3)
+                    : ((static_cast<uint32_t>(g) << 7) | (static_cast<uint32_t>(lane) << 2));
+  __half2 hacc[R][NT];
+#pragma unroll
+  for (int g = 0; g < R; ++g)
+#pragma unroll
+    for (int tk = 0; tk < NT; ++tk) hacc[g][tk] = __float2half2_rn(0.f);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    uint4 xv[NT];
+#pragma unroll
+    for (int tk = 0; tk < NT; ++tk) xv[tk] = lds128(xa + tk * kRecBytes + r * 16);
+#pragma unroll
+    for (int g = 0; g < R; ++g) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t off = __byte_perm(nb[g][r], lb[g], 0x6504 | (j << 4));
+        if (COMPACT) off >>= 1;
+        const __half2 w2 = *reinterpret_cast<const __half2*>(g_dsmem + off);
+#pragma unroll
+        for (int tk = 0; tk < NT; ++tk) {
+          const uint32_t xw = j == 0 ? xv[tk].x : j == 1 ? xv[tk].y : j == 2 ? xv[tk].z : xv[tk].w;
+          hacc[g][tk] = __hfma2(w2, *reinterpret_cast<const __half2*>(&xw), hacc[g][tk]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int tk = 0; tk < NT; ++tk) {
+    const float sc = *reinterpret_cast<const float*>(g_dsmem + xa + tk * kRecBytes + 64);
+#pragma unroll
+    for (int g = 0; g < R; ++g)
+      acc[g][tk] = __ffma2_rn(__half22float2(hacc[g][tk]), make_float2(sc, sc), acc[g][tk]);
+  }
+}
+
+template <int Q, int R, int NT, bool COMPACT>
+__device__ __forceinline__ void compute_column(uint32_t stage, int lane, const BitConsts& bc,
+                                               float2 (&acc)[R][NT]) {
+  if constexpr (Form<Q>::kPair) compute_column_pairs<Q, R, NT, COMPACT>(stage, lane, bc, acc);
+  else compute_column_bytes<Q, R, NT, COMPACT>(stage, lane, bc, acc);
+}
+
 // Start the copies of the warp's first kStages - 1 word columns (one commit
 // group each), so that their latency can overlap other set-up work.
 template <int Q, int R, int NT>
 __device__ __forceinline__ void ring_prime(const uint32_t* planes, long long plane_stride,
                                            long long N, const PassRows<R>& pr, int kw_lo,
-                                           int kw_hi, const float* const (&xs)[NT], int nt) {
+                                           int kw_hi, const char* const (&xs)[NT], int nt) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = kw_hi - kw_lo;
   if (n <= 0) return;
@@ -365,7 +578,7 @@ __device__ __forceinline__ void ring_prime(const uint32_t* planes, long long pla
 template <int Q, int R, int NT, bool COMPACT>
 __device__ __forceinline__ void rows_dot(const uint32_t* planes, long long plane_stride, long long N,
                                          const PassRows<R>& pr, int kw_lo, int kw_hi,
-                                         const float* const (&xs)[NT], int nt, const SmemPtrs& s,
+                                         const char* const (&xs)[NT], int nt, const SmemPtrs& s,
                                          const BitConsts& bc, float2 (&acc)[R][NT], bool primed) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -442,16 +655,18 @@ __global__ void wait_check_kernel(int32_t* status, uint32_t limit) {
 
 // ---------------------------------------------------------------- gate_up
 
-// One token group of one pass.  Paired passes (R = 2): slot 0 = gate rows
-// hcol0 + L, slot 1 = up rows I + hcol0 + L.  Compact passes (R = 1): lanes
-// 0-15 gate rows hcol0 + L, lanes 16-31 the matching up rows.
-template <int NT>
+// Activation rows of one token group, as byte pointers to word column 0 of
+// each token's row in the form of bitwidth Q.
+template <int Q, int NT>
 __device__ __forceinline__ void gateup_xs(const LayerArgs& a, const DecodeWs& w,
                                           const ExpertWork& ex, int g0, int nt,
-                                          const float* (&xs)[NT]) {
+                                          const char* (&xs)[NT]) {
 #pragma unroll
-  for (int tk = 0; tk < NT; ++tk)
-    xs[tk] = w.x32 + static_cast<long long>(w.perm[ex.off + g0 + min(tk, nt - 1)] / a.k) * a.H;
+  for (int tk = 0; tk < NT; ++tk) {
+    const long long row = w.perm[ex.off + g0 + min(tk, nt - 1)] / a.k;
+    xs[tk] = Form<Q>::kPair ? w.xp + row * (a.H / 32) * kRecBytes
+                            : reinterpret_cast<const char*>(w.xs + row * a.H);
+  }
 }
 
 template <int Q, int R, int NT>
@@ -461,9 +676,53 @@ __device__ void gateup_prime(const LayerArgs& a, const DecodeWs& w, const Expert
   const long long N = 2LL * a.I;
   int lo, hi;
   warp_range(KW, lo, hi);
-  const float* xs[NT];
-  gateup_xs<NT>(a, w, ex, g0, nt, xs);
+  const char* xs[NT];
+  gateup_xs<Q, NT>(a, w, ex, g0, nt, xs);
   ring_prime<Q, R, NT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt);
+}
+
+// Writes one token's h values of a tile (lane L holds column hcol0 + L for
+// L < width) in the form the expert's down block reads.  fp16 form needs the
+// largest magnitude of the 32 columns of a group: a paired pass (width 32)
+// has them all; compact passes (width 16) park the first half's values in
+// the fp32 buffer, and the second half's pass reads them back (the same
+// thread wrote them) and writes the whole record.
+__device__ __forceinline__ void store_h(const LayerArgs& a, const DecodeWs& w, int pos, int hcol0,
+                                        int width, int lane, float h, bool fp16_form) {
+  float* hs_row = w.hs + static_cast<long long>(pos) * a.I;
+  const int col = hcol0 + lane;
+  if (!fp16_form) {
+    if (lane < width) hs_row[(col & ~31) + byte_form_position(col & 31)] = h;
+    return;
+  }
+  const int group = hcol0 >> 5;
+  char* rec = w.hp + (static_cast<long long>(pos) * (a.I / 32) + group) * kRecBytes;
+  __half* vals = reinterpret_cast<__half*>(rec);
+  if (width == 32) {
+    float m = fabsf(h);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    const int e = group_exponent(m);
+    vals[nibble_form_position(col & 31)] = __float2half_rn(h * exp2i(-e));
+    if (lane == 0) *reinterpret_cast<float*>(rec + 64) = exp2i(e);
+    return;
+  }
+  if ((hcol0 & 31) == 0) {   // first half: park the values
+    if (lane < 16) hs_row[col] = h;
+    return;
+  }
+  const float h0 = lane < 16 ? hs_row[col - 16] : 0.f;
+  const float h1 = lane < 16 ? h : 0.f;
+  float m = fmaxf(fabsf(h0), fabsf(h1));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  const int e = group_exponent(m);
+  const float down = exp2i(-e);
+  if (lane < 16) {
+    vals[nibble_form_position((col - 16) & 31)] = __float2half_rn(h0 * down);
+    vals[nibble_form_position(col & 31)] = __float2half_rn(h1 * down);
+  }
+  if (lane == 0) *reinterpret_cast<float*>(rec + 64) = exp2i(e);
 }
 
 template <int Q, int R, bool COMPACT, int NT>
@@ -476,8 +735,8 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
   const long long N = 2LL * a.I;
   int lo, hi;
   warp_range(KW, lo, hi);
-  const float* xs[NT];
-  gateup_xs<NT>(a, w, ex, g0, nt, xs);
+  const char* xs[NT];
+  gateup_xs<Q, NT>(a, w, ex, g0, nt, xs);
   float2 acc[R][NT];
   rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc, primed);
   // the tile's last group claims the CTA's next tile; the atomic's round
@@ -490,7 +749,7 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
     for (int g = 0; g < R; ++g)
       s.red[((warp * kTG + tk) * 2 + g) * 32 + lane] = acc[g][tk].x + acc[g][tk].y;
   __syncthreads();
-  if (threadIdx.x < 32 * nt) {
+  if (threadIdx.x < 32 * nt) {   // warp tk finishes token tk
     const int tk = threadIdx.x >> 5;
     float v0 = 0.f, v1 = 0.f;
 #pragma unroll
@@ -500,10 +759,8 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
     }
     if (R == 1) v1 = __shfl_xor_sync(kFull, v0, 16);
     const int width = (R == 2) ? 32 : 16;
-    if (lane < width) {
-      const float h = v0 / (1.f + expf(-v0)) * v1;
-      w.h[static_cast<long long>(ex.off + g0 + tk) * a.I + hcol0 + lane] = h;
-    }
+    const float h = lane < width ? v0 / (1.f + expf(-v0)) * v1 : 0.f;
+    store_h(a, w, ex.off + g0 + tk, hcol0, width, lane, h, ent.q_other <= 4);
   }
   if (claim_counter && threadIdx.x == 0) s.misc[2] = claim;
   __syncthreads();
@@ -517,13 +774,13 @@ __device__ void gateup_pass(const LayerArgs& a, const DecodeWs& w, const ExpertW
   // the LUT loads go out first, then the first token group's first columns
   // (whose activation rows need one more dependent load), so that both
   // round trips overlap
-  LutPieces<Q, R> lp;
-  lut_fetch<Q, R>(ent.lut, pr, lp);
+  PassLut<Q, R> pl;
+  pass_lut_fetch<Q, R>(ent.lut, pr, pl);
   const int nt0 = min(kTG, ex.ne);
   if (nt0 == 1) gateup_prime<Q, R, 1>(a, w, ex, ent, pr, 0, nt0);
   else if (nt0 == 2) gateup_prime<Q, R, 2>(a, w, ex, ent, pr, 0, nt0);
   else gateup_prime<Q, R, 4>(a, w, ex, ent, pr, 0, nt0);
-  lut_store<Q, R, COMPACT>(lp);
+  pass_lut_store<Q, R, COMPACT>(pl, a.status);
   __syncthreads();
   for (int g0 = 0; g0 < ex.ne; g0 += kTG) {
     const int nt = min(kTG, ex.ne - g0);
@@ -535,18 +792,23 @@ __device__ void gateup_pass(const LayerArgs& a, const DecodeWs& w, const ExpertW
   }
 }
 
+// One row per lane for the bitwidths whose tables fill the LUT region.
+template <int Q>
+constexpr bool compact_q() { return Q == 4 || Q == 8; }
+
 template <int Q>
 __device__ void gateup_tile(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
                             const SlotInfo& ent, int i0, const SmemPtrs& s,
                             const BitConsts& bc, int* claim_counter) {
-  if (Q == 8) {
+  if constexpr (compact_q<Q>()) {
+    // two passes of 16 h columns: lanes 0-15 gate rows, lanes 16-31 up rows
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
       const int i = i0 + 16 * half;
       PassRows<1> pr;
       pr.seg[0][0] = i;
       pr.seg[0][1] = a.I + i;
-      gateup_pass<8, 1, true>(a, w, ex, ent, pr, i, s, bc, half ? claim_counter : nullptr);
+      gateup_pass<Q, 1, true>(a, w, ex, ent, pr, i, s, bc, half ? claim_counter : nullptr);
     }
   } else {
     PassRows<2> pr;
@@ -612,13 +874,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerA
 
 // ---------------------------------------------------------------- down
 
-template <int NT>
+template <int Q, int NT>
 __device__ __forceinline__ void down_xs(const LayerArgs& a, const DecodeWs& w,
                                         const ExpertWork& ex, int g0, int nt,
-                                        const float* (&xs)[NT]) {
+                                        const char* (&xs)[NT]) {
 #pragma unroll
-  for (int tk = 0; tk < NT; ++tk)
-    xs[tk] = w.h + static_cast<long long>(ex.off + g0 + min(tk, nt - 1)) * a.I;
+  for (int tk = 0; tk < NT; ++tk) {
+    const long long pos = ex.off + g0 + min(tk, nt - 1);
+    xs[tk] = Form<Q>::kPair ? w.hp + pos * (a.I / 32) * kRecBytes
+                            : reinterpret_cast<const char*>(w.hs + pos * a.I);
+  }
 }
 
 template <int Q, int R, int NT>
@@ -628,8 +893,8 @@ __device__ void down_prime(const LayerArgs& a, const DecodeWs& w, const ExpertWo
   const long long N = a.H;
   int lo, hi;
   warp_range(KW, lo, hi);
-  const float* xs[NT];
-  down_xs<NT>(a, w, ex, g0, nt, xs);
+  const char* xs[NT];
+  down_xs<Q, NT>(a, w, ex, g0, nt, xs);
   ring_prime<Q, R, NT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt);
 }
 
@@ -642,8 +907,8 @@ __device__ void down_group(const LayerArgs& a, const DecodeWs& w, const ExpertWo
   const long long N = a.H;
   int lo, hi;
   warp_range(KW, lo, hi);
-  const float* xs[NT];
-  down_xs<NT>(a, w, ex, g0, nt, xs);
+  const char* xs[NT];
+  down_xs<Q, NT>(a, w, ex, g0, nt, xs);
   float2 acc[R][NT];
   rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc, primed);
   // thread i < 32*R*nt (at most kThreads) writes row slot (i/32)%R of token
@@ -679,9 +944,9 @@ __device__ void down_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWor
   const bool early = a.I <= kEarlyDownMaxI;
   const int seen = (early && threadIdx.x == 0) ? load_relaxed(w.gu_done + ex.e) : 0;
   {  // the LUT does not depend on h
-    LutPieces<Q, R> lp;
-    lut_fetch<Q, R>(ent.lut, pr, lp);
-    lut_store<Q, R, COMPACT>(lp);
+    PassLut<Q, R> pl;
+    pass_lut_fetch<Q, R>(ent.lut, pr, pl);
+    pass_lut_store<Q, R, COMPACT>(pl, a.status);
   }
   if (!early) grid_dependency_wait();   // the whole gate_up grid is done
   else if (threadIdx.x == 0) wait_gate_up(w.gu_done + ex.e, seen, a.I / kPairsPerTile, a.status);
@@ -704,13 +969,13 @@ template <int Q>
 __device__ void down_tile(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
                           const SlotInfo& ent, int n0, int rows, const SmemPtrs& s,
                           const BitConsts& bc) {
-  if (Q == 8 || rows == 32) {
+  if (compact_q<Q>() || rows == 32) {
 #pragma unroll 1
     for (int grp = 0; grp < rows / 32; ++grp) {
       PassRows<1> pr;
       pr.seg[0][0] = n0 + 32 * grp;
       pr.seg[0][1] = n0 + 32 * grp + 16;
-      if (Q == 8) down_pass<8, 1, true>(a, w, ex, ent, pr, s, bc);
+      if constexpr (compact_q<Q>()) down_pass<Q, 1, true>(a, w, ex, ent, pr, s, bc);
       else down_pass<Q, 1, false>(a, w, ex, ent, pr, s, bc);
     }
   } else {
@@ -816,7 +1081,8 @@ __device__ __forceinline__ int q_class(int q) {
 
 // CTA 0: stable grouping of pairs by expert (offsets, perm), routed-expert
 // lists ordered by bitwidth class (largest first; order inside a class does
-// not matter), counters reset.  Other CTAs: hidden -> fp32 and out = 0.
+// not matter), counters reset.  Other CTAs: hidden -> both activation forms
+// (fp32, and fp16 records with their group scales) and out = 0.
 __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerArgs a,
                                                                    const DecodeWs w) {
   // when launched early (programmatic dependent launch), nothing of the
@@ -826,15 +1092,37 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
   allow_dependent_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (blockIdx.x != 0) {
+    // unit i = 4 columns; the 8 units of a group of 32 columns are 8
+    // consecutive lanes (H is a multiple of 32), and every lane of a warp
+    // runs every iteration, so the group maximum is a 3-step shuffle
     const long long n4 = static_cast<long long>(a.T) * a.H / 4;
     const long long stride = static_cast<long long>(gridDim.x - 1) * kPrepThreads;
-    for (long long i = static_cast<long long>(blockIdx.x - 1) * kPrepThreads + tid; i < n4;
-         i += stride) {
-      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.hidden) + i);
-      reinterpret_cast<float4*>(w.x32)[i] =
-          make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
-                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
-      reinterpret_cast<float4*>(a.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long base = static_cast<long long>(blockIdx.x - 1) * kPrepThreads; base < n4;
+         base += stride) {
+      const long long i = base + tid;
+      const bool valid = i < n4;
+      const uint2 raw = valid ? __ldg(reinterpret_cast<const uint2*>(a.hidden) + i) : make_uint2(0, 0);
+      const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                          __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+      float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      if (valid) {
+        const long long grp = i >> 3;          // (token, group of 32 columns)
+        const int u = static_cast<int>(i & 7);  // columns 4u .. 4u+3 of the group
+        float* xs_g = w.xs + grp * 32;
+        char* rec = w.xp + grp * kRecBytes;
+        const int e = group_exponent(m);
+        const float down = exp2i(-e);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          xs_g[byte_form_position(4 * u + j)] = v[j];
+          reinterpret_cast<__half*>(rec)[nibble_form_position(4 * u + j)] =
+              __float2half_rn(v[j] * down);
+        }
+        if (u == 0) *reinterpret_cast<float*>(rec + 64) = exp2i(e);
+        reinterpret_cast<float4*>(a.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
     return;
   }
@@ -939,7 +1227,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
       si.e = e;
       si.off = base[e];
       si.ne = count[e];
-      si.pad = 0;
+      si.q_other = dn.q;
       si.q = gu.q;
       si.planes = gu.planes;
       si.lut = gu.lut;
@@ -949,6 +1237,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
       // down tiles of an expert whose gate_up block cannot run write zeros
       // (their h is not valid); the error was latched by the gate_up tiles
       si.q = dn.q;
+      si.q_other = gu.q;
       si.planes = dn.planes;
       si.lut = dn.lut;
       si.err = !gu_ok ? -1
@@ -1000,14 +1289,16 @@ namespace {
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsSizes {
-  size_t x32, h, y, offsets, perm, routed, ctl, arrive, gu_done;
+  size_t xs, xp, hs, hp, y, offsets, perm, routed, ctl, arrive, gu_done;
 };
 
 WsSizes ws_sizes(const pw_moe_shape& s) {
   const size_t P = static_cast<size_t>(s.T) * s.k;
   WsSizes z;
-  z.x32 = round256(4 * static_cast<size_t>(s.T) * s.H);
-  z.h = round256(4 * P * s.I);
+  z.xs = round256(4 * static_cast<size_t>(s.T) * s.H);
+  z.xp = round256(kRecBytes * static_cast<size_t>(s.T) * (s.H / 32));
+  z.hs = round256(4 * P * s.I);
+  z.hp = round256(kRecBytes * P * (s.I / 32));
   z.y = round256(4 * P * s.H);
   z.offsets = round256(4 * (static_cast<size_t>(s.E) + 1));
   z.perm = round256(4 * P);
@@ -1045,14 +1336,15 @@ bool hybrid_possible(const pw_moe_shape& s) {
 
 }  // namespace
 
-// Workspace: x32 [T][H] | h [T*k][I] | y [T*k][H] fp32 | offsets [E+1] |
-// perm [T*k] | routed lists [E] x 2 | control words | arrival counters [H/32]
-// | gate_up tiles done [E] | (in calls of at least kHybridMinTokens tokens)
-// the GEMM kernels' scratch.
+// Workspace: hidden states [T][H] fp32 form | the same as fp16 records
+// [T][H/32] | h [T*k][I] fp32 form | h as fp16 records [T*k][I/32] | y
+// [T*k][H] fp32 | offsets [E+1] | perm [T*k] | routed lists [E] x 2 | control
+// words | arrival counters [H/32] | gate_up tiles done [E] | (in calls of at
+// least kHybridMinTokens tokens) the GEMM kernels' scratch.
 size_t decode_workspace_bytes(const pw_moe_shape& s, bool hybrid) {
   const WsSizes z = ws_sizes(s);
-  const size_t base =
-      z.x32 + z.h + z.y + z.offsets + z.perm + 2 * z.routed + z.ctl + z.arrive + z.gu_done;
+  const size_t base = z.xs + z.xp + z.hs + z.hp + z.y + z.offsets + z.perm + 2 * z.routed + z.ctl +
+                      z.arrive + z.gu_done;
   return base + ((hybrid && hybrid_possible(s)) ? heavy_scratch_bytes(s) : 0);
 }
 
@@ -1078,8 +1370,10 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
   const WsSizes z = ws_sizes(shape);
   char* p = static_cast<char*>(ws);
   DecodeWs w;
-  w.x32 = reinterpret_cast<float*>(p); p += z.x32;
-  w.h = reinterpret_cast<float*>(p); p += z.h;
+  w.xs = reinterpret_cast<float*>(p); p += z.xs;
+  w.xp = p; p += z.xp;
+  w.hs = reinterpret_cast<float*>(p); p += z.hs;
+  w.hp = p; p += z.hp;
   w.y = reinterpret_cast<float*>(p); p += z.y;
   w.offsets = reinterpret_cast<int*>(p); p += z.offsets;
   w.perm = reinterpret_cast<int*>(p); p += z.perm;

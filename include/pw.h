@@ -66,6 +66,9 @@ extern "C" {
 #define PW_ERR_CUDA               7  /* a CUDA runtime call failed                   */
 #define PW_ERR_TIMEOUT            8  /* a bounded device wait gave up                */
 #define PW_ERR_UNSUPPORTED_DEVICE 9  /* the current device is not sm_103             */
+#define PW_ERR_RANGE             10  /* device: a LUT value outside the range a block
+                                        committed at q <= 4 supports (|v| >= 2048 or
+                                        not finite); the block is still computed      */
 
 /* ---- page states of the Weight Page Table ------------------------------ */
 #define PW_PAGE_GPU          0  /* planes and LUT are in device memory        */
