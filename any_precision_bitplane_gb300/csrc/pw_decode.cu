@@ -139,7 +139,12 @@ struct SlotInfo {
                     // block, whose form decides how h is stored)
   const uint32_t* planes;
   const uint16_t* lut;
+  int32_t rows[4];  // hidden-state rows of the expert's first kTG pairs (the
+                    // last one repeated), so a pass's first copies need no
+                    // dependent load of perm
 };
+
+static_assert(sizeof(SlotInfo) == 56, "slot descriptor layout");
 
 // Workspace of one decode call.
 // Activations come in two forms, matching the two lookup forms (the column
@@ -307,6 +312,7 @@ template <int Q, int R>
 __device__ __forceinline__ void pair_lut_fetch(const uint16_t* lut, const PassRows<R>& pr,
                                                PairLutPieces<Q, R>& lp) {
   using L = PairLutPieces<Q, R>;
+  if (threadIdx.x >= 256) return;   // 256 threads build the tables
   const int rho = threadIdx.x / L::kTPR;
   const int g = rho >> 5, lane = rho & 31;
   const int row = seg_base<R>(pr, g, lane >> 4) + (lane & 15);
@@ -328,6 +334,7 @@ constexpr uint32_t kPairLutLimitBits = 0x6800u;   // fp16 2048
 template <int Q, int R, bool COMPACT>
 __device__ __forceinline__ void pair_lut_store(const PairLutPieces<Q, R>& lp, int32_t* status) {
   using L = PairLutPieces<Q, R>;
+  if (threadIdx.x >= 256) return;   // 256 threads build the tables
   const int rho = threadIdx.x / L::kTPR, c = threadIdx.x % L::kTPR;
   const int g = rho >> 5, lane = rho & 31;
   bool bad = false;
@@ -659,11 +666,11 @@ __global__ void wait_check_kernel(int32_t* status, uint32_t limit) {
 // each token's row in the form of bitwidth Q.
 template <int Q, int NT>
 __device__ __forceinline__ void gateup_xs(const LayerArgs& a, const DecodeWs& w,
-                                          const ExpertWork& ex, int g0, int nt,
+                                          const ExpertWork& ex, const SlotInfo& ent, int g0, int nt,
                                           const char* (&xs)[NT]) {
 #pragma unroll
   for (int tk = 0; tk < NT; ++tk) {
-    const long long row = w.perm[ex.off + g0 + min(tk, nt - 1)] / a.k;
+    const long long row = g0 == 0 ? ent.rows[tk] : w.perm[ex.off + g0 + min(tk, nt - 1)] / a.k;
     xs[tk] = Form<Q>::kPair ? w.xp + row * (a.H / 32) * kRecBytes
                             : reinterpret_cast<const char*>(w.xs + row * a.H);
   }
@@ -677,7 +684,7 @@ __device__ void gateup_prime(const LayerArgs& a, const DecodeWs& w, const Expert
   int lo, hi;
   warp_range(KW, lo, hi);
   const char* xs[NT];
-  gateup_xs<Q, NT>(a, w, ex, g0, nt, xs);
+  gateup_xs<Q, NT>(a, w, ex, ent, g0, nt, xs);
   ring_prime<Q, R, NT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt);
 }
 
@@ -736,7 +743,7 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
   int lo, hi;
   warp_range(KW, lo, hi);
   const char* xs[NT];
-  gateup_xs<Q, NT>(a, w, ex, g0, nt, xs);
+  gateup_xs<Q, NT>(a, w, ex, ent, g0, nt, xs);
   float2 acc[R][NT];
   rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc, primed);
   // the tile's last group claims the CTA's next tile; the atomic's round
@@ -778,17 +785,18 @@ __device__ void gateup_pass(const LayerArgs& a, const DecodeWs& w, const ExpertW
   pass_lut_fetch<Q, R>(ent.lut, pr, pl);
   const int nt0 = min(kTG, ex.ne);
   if (nt0 == 1) gateup_prime<Q, R, 1>(a, w, ex, ent, pr, 0, nt0);
-  else if (nt0 == 2) gateup_prime<Q, R, 2>(a, w, ex, ent, pr, 0, nt0);
-  else gateup_prime<Q, R, 4>(a, w, ex, ent, pr, 0, nt0);
+  else gateup_prime<Q, R, kTG>(a, w, ex, ent, pr, 0, nt0);
   pass_lut_store<Q, R, COMPACT>(pl, a.status);
   __syncthreads();
+  // token groups of one token take the one-token code; 2-4 tokens the kTG
+  // code, with the missing tokens zero-filled (fewer code variants keep the
+  // instruction cache warm)
   for (int g0 = 0; g0 < ex.ne; g0 += kTG) {
     const int nt = min(kTG, ex.ne - g0);
     const bool primed = (g0 == 0);
     int* cc = (g0 + kTG >= ex.ne) ? claim_counter : nullptr;
     if (nt == 1) gateup_group<Q, R, COMPACT, 1>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed, cc);
-    else if (nt == 2) gateup_group<Q, R, COMPACT, 2>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed, cc);
-    else gateup_group<Q, R, COMPACT, 4>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed, cc);
+    else gateup_group<Q, R, COMPACT, kTG>(a, w, ex, ent, pr, hcol0, g0, nt, s, bc, primed, cc);
   }
 }
 
@@ -953,14 +961,12 @@ __device__ void down_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWor
   __syncthreads();
   const int nt0 = min(kTG, ex.ne);
   if (nt0 == 1) down_prime<Q, R, 1>(a, w, ex, ent, pr, 0, nt0);
-  else if (nt0 == 2) down_prime<Q, R, 2>(a, w, ex, ent, pr, 0, nt0);
-  else down_prime<Q, R, 4>(a, w, ex, ent, pr, 0, nt0);
+  else down_prime<Q, R, kTG>(a, w, ex, ent, pr, 0, nt0);
   for (int g0 = 0; g0 < ex.ne; g0 += kTG) {
     const int nt = min(kTG, ex.ne - g0);
     const bool primed = (g0 == 0);
     if (nt == 1) down_group<Q, R, COMPACT, 1>(a, w, ex, ent, pr, g0, nt, s, bc, primed);
-    else if (nt == 2) down_group<Q, R, COMPACT, 2>(a, w, ex, ent, pr, g0, nt, s, bc, primed);
-    else down_group<Q, R, COMPACT, 4>(a, w, ex, ent, pr, g0, nt, s, bc, primed);
+    else down_group<Q, R, COMPACT, kTG>(a, w, ex, ent, pr, g0, nt, s, bc, primed);
   }
 }
 
@@ -1217,35 +1223,6 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
     }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kPrepThreads) {
-    if (count[e] > 0 && count[e] < heavy_min) {
-      const pw_block_entry gu = e == tid ? t_gu : a.table[2 * e];
-      const pw_block_entry dn = e == tid ? t_dn : a.table[2 * e + 1];
-      const bool gu_ok = gu.state == PW_PAGE_GPU && supported_q(gu.q);
-      const bool dn_ok = dn.state == PW_PAGE_GPU && supported_q(dn.q);
-      SlotInfo si;
-      si.e = e;
-      si.off = base[e];
-      si.ne = count[e];
-      si.q_other = dn.q;
-      si.q = gu.q;
-      si.planes = gu.planes;
-      si.lut = gu.lut;
-      si.err = gu_ok ? PW_OK
-                     : (gu.state != PW_PAGE_GPU ? PW_ERR_PAGE_NOT_RESIDENT : PW_ERR_UNSUPPORTED_Q);
-      w.routed_gu[atomicAdd(&s_bucket[0][q_class(gu.q)], 1)] = si;
-      // down tiles of an expert whose gate_up block cannot run write zeros
-      // (their h is not valid); the error was latched by the gate_up tiles
-      si.q = dn.q;
-      si.q_other = gu.q;
-      si.planes = dn.planes;
-      si.lut = dn.lut;
-      si.err = !gu_ok ? -1
-               : dn_ok ? PW_OK
-                       : (dn.state != PW_PAGE_GPU ? PW_ERR_PAGE_NOT_RESIDENT : PW_ERR_UNSUPPORTED_Q);
-      w.routed_dn[atomicAdd(&s_bucket[1][q_class(dn.q)], 1)] = si;
-    }
-  }
   // stable placement: rank among same-expert lanes (match), earlier warps of
   // the chunk (per-warp counts) and earlier chunks (running base)
   for (int c0 = 0; c0 < P; c0 += kPrepThreads) {
@@ -1271,6 +1248,40 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
       base[x] += add;
     }
     __syncthreads();
+  }
+  // slot descriptors, once the placement is done (perm is readable by the
+  // whole CTA after the loop's last barrier; base[e] has moved past e's
+  // pairs)
+  for (int e = tid; e < E; e += kPrepThreads) {
+    if (count[e] > 0 && count[e] < heavy_min) {
+      const pw_block_entry gu = e == tid ? t_gu : a.table[2 * e];
+      const pw_block_entry dn = e == tid ? t_dn : a.table[2 * e + 1];
+      const bool gu_ok = gu.state == PW_PAGE_GPU && supported_q(gu.q);
+      const bool dn_ok = dn.state == PW_PAGE_GPU && supported_q(dn.q);
+      SlotInfo si;
+      si.e = e;
+      si.off = base[e] - count[e];
+      si.ne = count[e];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) si.rows[i] = w.perm[si.off + min(i, si.ne - 1)] / a.k;
+      si.q_other = dn.q;
+      si.q = gu.q;
+      si.planes = gu.planes;
+      si.lut = gu.lut;
+      si.err = gu_ok ? PW_OK
+                     : (gu.state != PW_PAGE_GPU ? PW_ERR_PAGE_NOT_RESIDENT : PW_ERR_UNSUPPORTED_Q);
+      w.routed_gu[atomicAdd(&s_bucket[0][q_class(gu.q)], 1)] = si;
+      // down tiles of an expert whose gate_up block cannot run write zeros
+      // (their h is not valid); the error was latched by the gate_up tiles
+      si.q = dn.q;
+      si.q_other = gu.q;
+      si.planes = dn.planes;
+      si.lut = dn.lut;
+      si.err = !gu_ok ? -1
+               : dn_ok ? PW_OK
+                       : (dn.state != PW_PAGE_GPU ? PW_ERR_PAGE_NOT_RESIDENT : PW_ERR_UNSUPPORTED_Q);
+      w.routed_dn[atomicAdd(&s_bucket[1][q_class(dn.q)], 1)] = si;
+    }
   }
 }
 
