@@ -34,6 +34,10 @@ PATH_AUTO = 0
 PATH_DECODE = 1
 PATH_PREFILL = 2
 
+INDEX_NIBBLES = 0
+INDEX_BYTES = 1
+INDEX_HALVES = 2
+
 BITWIDTHS = (3, 4, 5, 6, 8)
 
 
@@ -82,6 +86,9 @@ _SIGNATURES = {
     "pw_page_table_commit_after": (_c.c_int, [_P, _I32, _P, _P, _P, _P, _P]),
     "pw_plan_recommit": (_c.c_int, [_I32, _P, _P, _P, _P, _I32, _c.c_int64, _P, _P, _P, _P]),
     "pw_debug_bounded_wait": (_c.c_int, [_P, _I32, _I32, _P]),
+    "pw_debug_index": (_c.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P]),
+    "pw_debug_dequant": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]),
+    "pw_debug_workspace_section": (_c.c_int, [_P, _I32, _I32, _P, _P]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -325,6 +332,39 @@ def debug_bounded_wait(table, which, polls, stream=None):
     limit; it latches PW_ERR_TIMEOUT in the table's status word."""
     _check(lib().pw_debug_bounded_wait(table.handle, int(which), int(polls), _stream(stream)),
            "pw_debug_bounded_wait")
+
+
+def debug_index(planes, N, K, q, form, idx=None, stream=None):
+    """The kernels' own index extraction (form INDEX_NIBBLES / INDEX_BYTES /
+    INDEX_HALVES) on a block: uint8 [N, K], column order restored."""
+    _need_cuda(planes)
+    if idx is None:
+        idx = torch.empty((N, K), dtype=torch.uint8, device=planes.device)
+    _check(lib().pw_debug_index(_ptr(planes), N, K, q, form, _ptr(idx), _stream(stream)),
+           "pw_debug_index")
+    return idx
+
+
+def debug_dequant(planes, lut, N, K, q, path, table=None, out=None, stream=None):
+    """The kernels' own table build and lookup on a block (path PATH_DECODE or
+    PATH_PREFILL): float32 [N, K]."""
+    _need_cuda(planes, lut)
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=planes.device)
+    _check(lib().pw_debug_dequant(_ptr(planes), _ptr(lut), N, K, q, path, _ptr(out),
+                                  table.handle if table is not None else None, _stream(stream)),
+           "pw_debug_dequant")
+    return out
+
+
+def debug_workspace_section(T, H, I, E, k, path, section):
+    """(offset, bytes) of a section of a forward call's workspace."""
+    s = MoeShape(T, H, I, E, k)
+    off = ctypes.c_size_t(0)
+    n = ctypes.c_size_t(0)
+    _check(lib().pw_debug_workspace_section(ctypes.byref(s), path, section, ctypes.byref(off),
+                                            ctypes.byref(n)), "pw_debug_workspace_section")
+    return off.value, n.value
 
 
 def set_timing_events(before=None, after=None):

@@ -473,6 +473,57 @@ int pw_debug_bounded_wait(pw_page_table* table, int32_t which, int32_t polls,
   return e == cudaSuccess ? PW_OK : cuda_fail(e, "bounded-wait check launch");
 }
 
+int pw_debug_index(const uint32_t* planes, int32_t N, int32_t K, int32_t q, int32_t form,
+                   uint8_t* idx, cudaStream_t stream) {
+  if (N < 0) return fail(PW_ERR_INVALID_ARG, "N < 0");
+  if (K <= 0 || K % 32) return fail(PW_ERR_SHAPE, "K (%d) must be a positive multiple of 32", K);
+  if (!pw::supported_q_host(q)) return fail(PW_ERR_UNSUPPORTED_Q, "q = %d is not in {3,4,5,6,8}", q);
+  if (form < PW_INDEX_NIBBLES || form > PW_INDEX_HALVES)
+    return fail(PW_ERR_INVALID_ARG, "unknown index form %d", form);
+  if (form == PW_INDEX_NIBBLES && q > 4)
+    return fail(PW_ERR_UNSUPPORTED_Q, "nibble indices hold q <= 4 (got %d)", q);
+  if (N == 0) return PW_OK;
+  if (!planes || !idx) return fail(PW_ERR_INVALID_ARG, "NULL pointer");
+  int rc = pw::check_device();
+  if (rc) return rc;
+  const cudaError_t e =
+      form == PW_INDEX_HALVES ? pw::launch_half_index_check(planes, N, K, q, idx, stream)
+                              : pw::launch_index_check(planes, N, K, q, form == PW_INDEX_NIBBLES, idx, stream);
+  return e == cudaSuccess ? PW_OK : cuda_fail(e, "index check launch");
+}
+
+int pw_debug_dequant(const uint32_t* planes, const uint16_t* lut, int32_t N, int32_t K, int32_t q,
+                     int32_t path, float* w, pw_page_table* table, cudaStream_t stream) {
+  if (N < 0) return fail(PW_ERR_INVALID_ARG, "N < 0");
+  if (K <= 0 || K % 32) return fail(PW_ERR_SHAPE, "K (%d) must be a positive multiple of 32", K);
+  if (N % 32) return fail(PW_ERR_SHAPE, "N (%d) must be a multiple of 32", N);
+  if (!pw::supported_q_host(q)) return fail(PW_ERR_UNSUPPORTED_Q, "q = %d is not in {3,4,5,6,8}", q);
+  if (path != PW_PATH_DECODE && path != PW_PATH_PREFILL)
+    return fail(PW_ERR_INVALID_ARG, "path must be PW_PATH_DECODE or PW_PATH_PREFILL");
+  if (N == 0) return PW_OK;
+  if (!planes || !lut || !w) return fail(PW_ERR_INVALID_ARG, "NULL pointer");
+  if (!pw::aligned(lut, 16)) return fail(PW_ERR_INVALID_ARG, "lut must be 16-byte aligned");
+  int rc = pw::check_device();
+  if (rc) return rc;
+  const cudaError_t e =
+      path == PW_PATH_PREFILL
+          ? pw::launch_half_dequant_check(planes, lut, N, K, q, w, stream)
+          : pw::launch_dequant_check(planes, lut, N, K, q, w, table ? table->d_status : nullptr, stream);
+  return e == cudaSuccess ? PW_OK : cuda_fail(e, "dequant check launch");
+}
+
+int pw_debug_workspace_section(const pw_moe_shape* shape, int32_t path, int32_t section,
+                               size_t* offset, size_t* bytes) {
+  int rc = pw::check_shape(shape);
+  if (rc) return rc;
+  if (!offset || !bytes) return fail(PW_ERR_INVALID_ARG, "NULL pointer");
+  if (path != PW_PATH_DECODE && path != PW_PATH_PREFILL)
+    return fail(PW_ERR_INVALID_ARG, "path must be PW_PATH_DECODE or PW_PATH_PREFILL");
+  const int r = path == PW_PATH_DECODE ? pw::decode_ws_section(*shape, section, offset, bytes)
+                                       : pw::prefill_ws_section(*shape, section, offset, bytes);
+  return r == 0 ? PW_OK : fail(PW_ERR_INVALID_ARG, "unknown workspace section %d", section);
+}
+
 int32_t pw_prefill_min_pairs(const pw_moe_shape* shape) {
   if (pw::check_shape(shape)) return -1;
   return pw::prefill_min_pairs(*shape);

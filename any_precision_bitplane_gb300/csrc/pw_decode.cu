@@ -62,6 +62,7 @@
 // q = 4 and q = 8 blocks stream one row per lane so that their tables fit.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "pw_bits.cuh"
@@ -151,9 +152,10 @@ static_assert(sizeof(SlotInfo) == 56, "slot descriptor layout");
 // order inside each group of 32 is the one the index form produces):
 //   fp32 form  float [rows][K], column c of a group at byte_form_position(c);
 //   fp16 form  one 80-byte record per (row, group of 32 columns): 32 fp16
-//              values x * 2^-e at nibble_form_position(c), then the float
-//              2^e at byte 64 (e puts the group's largest |x * 2^-e| in
-//              [1, 2)), then padding.
+//              values x * 2^-e at nibble_form_position(c), where e is that of
+//              the column's half of the group (columns 0-15 or 16-31: e puts
+//              the half's largest |x * 2^-e| in [1, 2)); then the floats 2^e
+//              of the two halves at bytes 64 and 68, then padding.
 constexpr int kRecBytes = 80;
 
 struct DecodeWs {
@@ -448,6 +450,22 @@ __device__ __forceinline__ uint4 lds128(uint32_t off) {
   return *reinterpret_cast<const uint4*>(g_dsmem + off);
 }
 
+// Lane L's base offset in the LUT region for row slot g, and the offset of
+// the table entry that byte j of an index word selects (one byte permute; in
+// the compact layout entries are 128 bytes apart, so the permute's v * 256 +
+// 8L is halved).  Shared by the column loops and the lookup check.
+template <bool COMPACT>
+__device__ __forceinline__ uint32_t lane_base(int g, int lane) {
+  return COMPACT ? (static_cast<uint32_t>(lane) << 3)
+                 : ((static_cast<uint32_t>(g) << 7) | (static_cast<uint32_t>(lane) << 2));
+}
+
+template <bool COMPACT>
+__device__ __forceinline__ uint32_t lut_offset(uint32_t word, uint32_t lb, int j) {
+  const uint32_t off = __byte_perm(word, lb, 0x6504 | (j << 4));
+  return COMPACT ? off >> 1 : off;
+}
+
 // One word column from a ring stage, fp32 tables (Q = 5, 6, 8): byte indices
 // of each row, one lookup per weight, packed fp32 products.  B[r] byte b is
 // column 8b + r, whose activation sits at position 4r + b: the float4 at 4r.
@@ -466,9 +484,7 @@ __device__ __forceinline__ void compute_column_bytes(uint32_t stage, int lane, c
   const uint32_t xa = stage + kStagePlaneBytes;
   uint32_t lb[R];
 #pragma unroll
-  for (int g = 0; g < R; ++g)
-    lb[g] = COMPACT ? (static_cast<uint32_t>(lane) << 3)
-                    : ((static_cast<uint32_t>(g) << 7) | (static_cast<uint32_t>(lane) << 2));
+  for (int g = 0; g < R; ++g) lb[g] = lane_base<COMPACT>(g, lane);
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     float4 xv[NT];
@@ -482,11 +498,8 @@ __device__ __forceinline__ void compute_column_bytes(uint32_t stage, int lane, c
     for (int g = 0; g < R; ++g) {
       float w[4];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        uint32_t off = __byte_perm(ib[g][r], lb[g], 0x6504 | (b << 4));
-        if (COMPACT) off >>= 1;
-        w[b] = *reinterpret_cast<const float*>(g_dsmem + off);
-      }
+      for (int b = 0; b < 4; ++b)
+        w[b] = *reinterpret_cast<const float*>(g_dsmem + lut_offset<COMPACT>(ib[g][r], lb[g], b));
 #pragma unroll
       for (int tk = 0; tk < NT; ++tk) {
         acc[g][tk] = __ffma2_rn(make_float2(w[0], w[1]), make_float2(xv[tk].x, xv[tk].y), acc[g][tk]);
@@ -499,9 +512,9 @@ __device__ __forceinline__ void compute_column_bytes(uint32_t stage, int lane, c
 // One word column from a ring stage, pair tables (Q = 3, 4): nibble indices
 // of each row; byte j of N[r] pairs columns 8j + r and 8j + 4 + r, whose
 // fp16 activations sit at positions 8r + 2j and 8r + 2j + 1: half2 j of the
-// 16 bytes at 16r of the token's record.  The fp16 products of the column's
-// 16 pairs are summed in a half2, which is then added to the fp32
-// accumulator with the group's scale 2^e.
+// 16 bytes at 16r of the token's record.  The fp16 products of each half of
+// the word column (8 pairs) are summed in a half2, which is then added to the
+// fp32 accumulator with that half's scale 2^e.
 template <int Q, int R, int NT, bool COMPACT>
 __device__ __forceinline__ void compute_column_pairs(uint32_t stage, int lane, const BitConsts& bc,
                                                      float2 (&acc)[R][NT]) {
@@ -517,14 +530,16 @@ __device__ __forceinline__ void compute_column_pairs(uint32_t stage, int lane, c
   const uint32_t xa = stage + kStagePlaneBytes;
   uint32_t lb[R];
 #pragma unroll
-  for (int g = 0; g < R; ++g)
-    lb[g] = COMPACT ? (static_cast<uint32_t>(lane) << 3)
-                    : ((static_cast<uint32_t>(g) << 7) | (static_cast<uint32_t>(lane) << 2));
-  __half2 hacc[R][NT];
+  for (int g = 0; g < R; ++g) lb[g] = lane_base<COMPACT>(g, lane);
+  // byte j of N[r] holds columns 8j + r and 8j + 4 + r: j < 2 is the first
+  // half of the word column (columns 0-15), j >= 2 the second
+  __half2 hacc[2][R][NT];
 #pragma unroll
-  for (int g = 0; g < R; ++g)
+  for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-    for (int tk = 0; tk < NT; ++tk) hacc[g][tk] = __float2half2_rn(0.f);
+    for (int g = 0; g < R; ++g)
+#pragma unroll
+      for (int tk = 0; tk < NT; ++tk) hacc[hf][g][tk] = __float2half2_rn(0.f);
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     uint4 xv[NT];
@@ -534,23 +549,24 @@ __device__ __forceinline__ void compute_column_pairs(uint32_t stage, int lane, c
     for (int g = 0; g < R; ++g) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        uint32_t off = __byte_perm(nb[g][r], lb[g], 0x6504 | (j << 4));
-        if (COMPACT) off >>= 1;
-        const __half2 w2 = *reinterpret_cast<const __half2*>(g_dsmem + off);
+        const __half2 w2 =
+            *reinterpret_cast<const __half2*>(g_dsmem + lut_offset<COMPACT>(nb[g][r], lb[g], j));
 #pragma unroll
         for (int tk = 0; tk < NT; ++tk) {
           const uint32_t xw = j == 0 ? xv[tk].x : j == 1 ? xv[tk].y : j == 2 ? xv[tk].z : xv[tk].w;
-          hacc[g][tk] = __hfma2(w2, *reinterpret_cast<const __half2*>(&xw), hacc[g][tk]);
+          hacc[j >> 1][g][tk] = __hfma2(w2, *reinterpret_cast<const __half2*>(&xw), hacc[j >> 1][g][tk]);
         }
       }
     }
   }
 #pragma unroll
   for (int tk = 0; tk < NT; ++tk) {
-    const float sc = *reinterpret_cast<const float*>(g_dsmem + xa + tk * kRecBytes + 64);
+    const float2 sc = *reinterpret_cast<const float2*>(g_dsmem + xa + tk * kRecBytes + 64);
 #pragma unroll
-    for (int g = 0; g < R; ++g)
-      acc[g][tk] = __ffma2_rn(__half22float2(hacc[g][tk]), make_float2(sc, sc), acc[g][tk]);
+    for (int g = 0; g < R; ++g) {
+      acc[g][tk] = __ffma2_rn(__half22float2(hacc[0][g][tk]), make_float2(sc.x, sc.x), acc[g][tk]);
+      acc[g][tk] = __ffma2_rn(__half22float2(hacc[1][g][tk]), make_float2(sc.y, sc.y), acc[g][tk]);
+    }
   }
 }
 
@@ -688,48 +704,29 @@ __device__ void gateup_prime(const LayerArgs& a, const DecodeWs& w, const Expert
   ring_prime<Q, R, NT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt);
 }
 
-// Writes one token's h values of a tile (lane L holds column hcol0 + L for
-// L < width) in the form the expert's down block reads.  fp16 form needs the
-// largest magnitude of the 32 columns of a group: a paired pass (width 32)
-// has them all; compact passes (width 16) park the first half's values in
-// the fp32 buffer, and the second half's pass reads them back (the same
-// thread wrote them) and writes the whole record.
+// Writes one token's h values of a pass (lane L holds column hcol0 + L for
+// L < width) in the form the expert's down block reads.  The fp16 form's
+// scale belongs to a half of the group of 32 columns (16 columns), which a
+// compact pass (width 16) covers alone and a paired pass (width 32) covers
+// with lanes 0-15 and 16-31.
 __device__ __forceinline__ void store_h(const LayerArgs& a, const DecodeWs& w, int pos, int hcol0,
                                         int width, int lane, float h, bool fp16_form) {
-  float* hs_row = w.hs + static_cast<long long>(pos) * a.I;
   const int col = hcol0 + lane;
   if (!fp16_form) {
+    float* hs_row = w.hs + static_cast<long long>(pos) * a.I;
     if (lane < width) hs_row[(col & ~31) + byte_form_position(col & 31)] = h;
     return;
   }
-  const int group = hcol0 >> 5;
-  char* rec = w.hp + (static_cast<long long>(pos) * (a.I / 32) + group) * kRecBytes;
-  __half* vals = reinterpret_cast<__half*>(rec);
-  if (width == 32) {
-    float m = fabsf(h);
+  char* rec = w.hp + (static_cast<long long>(pos) * (a.I / 32) + (hcol0 >> 5)) * kRecBytes;
+  float m = lane < width ? fabsf(h) : 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    const int e = group_exponent(m);
-    vals[nibble_form_position(col & 31)] = __float2half_rn(h * exp2i(-e));
-    if (lane == 0) *reinterpret_cast<float*>(rec + 64) = exp2i(e);
-    return;
-  }
-  if ((hcol0 & 31) == 0) {   // first half: park the values
-    if (lane < 16) hs_row[col] = h;
-    return;
-  }
-  const float h0 = lane < 16 ? hs_row[col - 16] : 0.f;
-  const float h1 = lane < 16 ? h : 0.f;
-  float m = fmaxf(fabsf(h0), fabsf(h1));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
   const int e = group_exponent(m);
-  const float down = exp2i(-e);
-  if (lane < 16) {
-    vals[nibble_form_position((col - 16) & 31)] = __float2half_rn(h0 * down);
-    vals[nibble_form_position(col & 31)] = __float2half_rn(h1 * down);
+  if (lane < width) {
+    reinterpret_cast<__half*>(rec)[nibble_form_position(col & 31)] = __float2half_rn(h * exp2i(-e));
+    if ((lane & 15) == 0)
+      *reinterpret_cast<float*>(rec + 64 + 4 * ((col >> 4) & 1)) = exp2i(e);
   }
-  if (lane == 0) *reinterpret_cast<float*>(rec + 64) = exp2i(e);
 }
 
 template <int Q, int R, bool COMPACT, int NT>
@@ -1100,7 +1097,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
   if (blockIdx.x != 0) {
     // unit i = 4 columns; the 8 units of a group of 32 columns are 8
     // consecutive lanes (H is a multiple of 32), and every lane of a warp
-    // runs every iteration, so the group maximum is a 3-step shuffle
+    // runs every iteration, so a half's maximum (4 units) is a 2-step shuffle
     const long long n4 = static_cast<long long>(a.T) * a.H / 4;
     const long long stride = static_cast<long long>(gridDim.x - 1) * kPrepThreads;
     for (long long base = static_cast<long long>(blockIdx.x - 1) * kPrepThreads; base < n4;
@@ -1112,7 +1109,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
                           __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
       float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
-      for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      for (int o = 1; o < 4; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));   // a half: 16 columns
       if (valid) {
         const long long grp = i >> 3;          // (token, group of 32 columns)
         const int u = static_cast<int>(i & 7);  // columns 4u .. 4u+3 of the group
@@ -1126,7 +1123,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
           reinterpret_cast<__half*>(rec)[nibble_form_position(4 * u + j)] =
               __float2half_rn(v[j] * down);
         }
-        if (u == 0) *reinterpret_cast<float*>(rec + 64) = exp2i(e);
+        if ((u & 3) == 0) *reinterpret_cast<float*>(rec + 64 + 4 * (u >> 2)) = exp2i(e);
         reinterpret_cast<float4*>(a.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
@@ -1292,6 +1289,190 @@ cudaError_t launch_wait_check_decode(int32_t* status, uint32_t polls, cudaStream
   return cudaGetLastError();
 }
 
+namespace {
+// The >48 KB shared-memory opt-in of the decode kernels, set once per device.
+cudaError_t configure_decode() {
+  cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kSmemBytes));
+}
+}  // namespace
+
+namespace {
+
+// ---------------------------------------------------------------- checks
+//
+// The decode kernels' index extraction and table lookups, run on a whole
+// block and written back in column order, so that they can be compared bit
+// for bit with the format's definition.  The column order of each index
+// form is the one the kernels' activation layouts assume.
+
+// One thread per (row n, word column w): the q plane words, the kernels'
+// extraction, each index stored at its column.
+template <int Q, bool NIBBLES>
+__global__ void __launch_bounds__(256) index_check_kernel(const uint32_t* __restrict__ planes, int N,
+                                                          int KW, uint8_t* __restrict__ idx,
+                                                          const BitConsts bc) {
+  const long long total = static_cast<long long>(N) * KW;
+  const long long plane = total;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long wcol = i / N, n = i % N;
+    uint32_t P[Q];
+#pragma unroll
+    for (int p = 0; p < Q; ++p) P[p] = planes[p * plane + wcol * N + n];
+    uint8_t* row = idx + n * (32LL * KW) + 32 * wcol;
+    if constexpr (NIBBLES) {
+      uint32_t nb[4];
+      planes_to_nibbles<Q>(P, nb, bc);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) row[4 * m + r] = static_cast<uint8_t>((nb[r] >> (4 * m)) & 15u);
+    } else {
+      uint32_t b8[8];
+      planes_to_bytes<Q>(P, b8, bc);
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) row[8 * b + r] = static_cast<uint8_t>((b8[r] >> (8 * b)) & 255u);
+    }
+  }
+}
+
+// One CTA (kThreads) per pass of rows, as the gate_up / down kernels run it:
+// 64 rows in two slots, or 32 rows in one (compact bitwidths, or a ragged
+// last 32 rows).  The pass's table is built with the kernels' fetch and
+// store, then lane L of a slot looks up its row's indices with the kernels'
+// offsets and writes each weight at its column (pair tables give two).
+template <int Q, int R, bool COMPACT>
+__device__ void dequant_check_pass(const uint32_t* planes, const uint16_t* lut, int N, int KW,
+                                   int n0, float* out, const BitConsts& bc, int32_t* status) {
+  PassRows<R> pr;
+  pr.seg[0][0] = n0;
+  pr.seg[0][1] = n0 + 16;
+  if (R == 2) {
+    pr.seg[R - 1][0] = n0 + 32;
+    pr.seg[R - 1][1] = n0 + 48;
+  }
+  __syncthreads();   // the previous pass is done with the table
+  {
+    PassLut<Q, R> pl;
+    pass_lut_fetch<Q, R>(lut, pr, pl);
+    pass_lut_store<Q, R, COMPACT>(pl, status);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long plane = static_cast<long long>(N) * KW;
+  for (int wcol = warp; wcol < KW; wcol += kWarps) {
+#pragma unroll
+    for (int g = 0; g < R; ++g) {
+      const int row = seg_base<R>(pr, g, lane >> 4) + (lane & 15);
+      uint32_t P[Q];
+#pragma unroll
+      for (int p = 0; p < Q; ++p) P[p] = planes[p * plane + static_cast<long long>(wcol) * N + row];
+      const uint32_t lb = lane_base<COMPACT>(g, lane);
+      float* dst = out + static_cast<long long>(row) * (32LL * KW) + 32 * wcol;
+      if constexpr (Form<Q>::kPair) {
+        uint32_t nb[4];
+        planes_to_nibbles<Q>(P, nb, bc);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const __half2 w2 = *reinterpret_cast<const __half2*>(g_dsmem + lut_offset<COMPACT>(nb[r], lb, j));
+            dst[8 * j + r] = __low2float(w2);        // low nibble: column 8j + r
+            dst[8 * j + 4 + r] = __high2float(w2);   // high nibble: column 8j + 4 + r
+          }
+      } else {
+        uint32_t b8[8];
+        planes_to_bytes<Q>(P, b8, bc);
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            dst[8 * b + r] = *reinterpret_cast<const float*>(g_dsmem + lut_offset<COMPACT>(b8[r], lb, b));
+      }
+    }
+  }
+}
+
+template <int Q>
+__global__ void __launch_bounds__(kThreads, 1) dequant_check_kernel(const uint32_t* planes,
+                                                                     const uint16_t* lut, int N,
+                                                                     int KW, float* out,
+                                                                     const BitConsts bc,
+                                                                     int32_t* status) {
+  constexpr bool C = compact_q<Q>();
+  for (int n0 = blockIdx.x * 64; n0 < N; n0 += gridDim.x * 64) {
+    const int rows = min(64, N - n0);   // 64, or 32 on a ragged last pass
+    if (C || rows == 32) {
+      for (int grp = 0; grp < rows / 32; ++grp)
+        dequant_check_pass<Q, 1, C>(planes, lut, N, KW, n0 + 32 * grp, out, bc, status);
+    } else if constexpr (!C) {
+      dequant_check_pass<Q, 2, false>(planes, lut, N, KW, n0, out, bc, status);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_index_check(const uint32_t* planes, int N, int K, int q, bool nibbles,
+                               uint8_t* idx, cudaStream_t s) {
+  const BitConsts bc = make_bit_consts();
+  const long long total = static_cast<long long>(N) * (K / 32);
+  const int grid = static_cast<int>(std::min<long long>((total + 255) / 256, 64LL * sm_count()));
+  const int KW = K / 32;
+#define PW_IDX(QQ, NB) index_check_kernel<QQ, NB><<<grid, 256, 0, s>>>(planes, N, KW, idx, bc)
+  if (nibbles) {
+    switch (q) {
+      case 3: PW_IDX(3, true); break;
+      case 4: PW_IDX(4, true); break;
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    switch (q) {
+      case 3: PW_IDX(3, false); break;
+      case 4: PW_IDX(4, false); break;
+      case 5: PW_IDX(5, false); break;
+      case 6: PW_IDX(6, false); break;
+      case 8: PW_IDX(8, false); break;
+      default: return cudaErrorInvalidValue;
+    }
+  }
+#undef PW_IDX
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_check(const uint32_t* planes, const uint16_t* lut, int N, int K, int q,
+                                 float* out, int32_t* status, cudaStream_t s) {
+  cudaError_t e = setup_once(kSetupDecode, configure_decode);
+  if (e != cudaSuccess) return e;
+  const BitConsts bc = make_bit_consts();
+  const int KW = K / 32;
+  const int grid = std::min((N + 63) / 64, 2 * sm_count());
+#define PW_DQ(QQ)                                                                              \
+  do {                                                                                         \
+    e = cudaFuncSetAttribute(dequant_check_kernel<QQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             static_cast<int>(kSmemBytes));                                    \
+    if (e != cudaSuccess) return e;                                                            \
+    dequant_check_kernel<QQ><<<grid, kThreads, kSmemBytes, s>>>(planes, lut, N, KW, out, bc, status); \
+  } while (0)
+  switch (q) {
+    case 3: PW_DQ(3); break;
+    case 4: PW_DQ(4); break;
+    case 5: PW_DQ(5); break;
+    case 6: PW_DQ(6); break;
+    case 8: PW_DQ(8); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef PW_DQ
+  return cudaGetLastError();
+}
+
 int decode_max_pairs() { return kMaxPairs; }
 int decode_max_experts() { return kMaxExperts; }
 
@@ -1347,6 +1528,21 @@ bool hybrid_possible(const pw_moe_shape& s) {
 
 }  // namespace
 
+// Byte ranges of a decode workspace a caller may read back (test hooks):
+// 0 offsets, 1 perm, 2 hidden states in fp32 form, 3 in fp16 records.
+int decode_ws_section(const pw_moe_shape& shape, int section, size_t* offset, size_t* bytes) {
+  const WsSizes z = ws_sizes(shape);
+  const size_t starts[5] = {0, z.xs, z.xs + z.xp, z.xs + z.xp + z.hs, z.xs + z.xp + z.hs + z.hp};
+  const size_t off_offsets = starts[4] + z.y;
+  switch (section) {
+    case 0: *offset = off_offsets; *bytes = 4 * (static_cast<size_t>(shape.E) + 1); return 0;
+    case 1: *offset = off_offsets + z.offsets; *bytes = 4 * static_cast<size_t>(shape.T) * shape.k; return 0;
+    case 2: *offset = 0; *bytes = 4 * static_cast<size_t>(shape.T) * shape.H; return 0;
+    case 3: *offset = z.xs; *bytes = kRecBytes * static_cast<size_t>(shape.T) * (shape.H / 32); return 0;
+    default: return -1;
+  }
+}
+
 // Workspace: hidden states [T][H] fp32 form | the same as fp16 records
 // [T][H/32] | h [T*k][I] fp32 form | h as fp16 records [T*k][I/32] | y
 // [T*k][H] fp32 | offsets [E+1] | perm [T*k] | routed lists [E] x 2 | control
@@ -1358,18 +1554,6 @@ size_t decode_workspace_bytes(const pw_moe_shape& s, bool hybrid) {
                       z.arrive + z.gu_done;
   return base + ((hybrid && hybrid_possible(s)) ? heavy_scratch_bytes(s) : 0);
 }
-
-namespace {
-// The >48 KB shared-memory opt-in of the decode kernels, set once per device.
-cudaError_t configure_decode() {
-  cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmemBytes));
-}
-}  // namespace
 
 cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, bool hybrid) {
   cudaError_t e0 = setup_once(kSetupDecode, configure_decode);

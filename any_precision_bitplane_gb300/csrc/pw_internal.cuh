@@ -131,6 +131,20 @@ size_t heavy_scratch_bytes(const pw_moe_shape& s);
 cudaError_t launch_heavy(const LayerArgs& a, const int32_t* offsets, const int32_t* perm, float* y,
                          void* scratch, int min_tokens, cudaStream_t s);
 
+// Bit-exact checks of the kernels' own index extraction and table lookups
+// (pw_debug_index / pw_debug_dequant), and the byte ranges of a workspace a
+// test may read back (pw_debug_workspace_section).
+cudaError_t launch_index_check(const uint32_t* planes, int N, int K, int q, bool nibbles,
+                               uint8_t* idx, cudaStream_t s);
+cudaError_t launch_dequant_check(const uint32_t* planes, const uint16_t* lut, int N, int K, int q,
+                                 float* out, int32_t* status, cudaStream_t s);
+cudaError_t launch_half_index_check(const uint32_t* planes, int N, int K, int q, uint8_t* idx,
+                                    cudaStream_t s);
+cudaError_t launch_half_dequant_check(const uint32_t* planes, const uint16_t* lut, int N, int K,
+                                      int q, float* out, cudaStream_t s);
+int decode_ws_section(const pw_moe_shape& shape, int section, size_t* offset, size_t* bytes);
+int prefill_ws_section(const pw_moe_shape& shape, int section, size_t* offset, size_t* bytes);
+
 // Failure-detection checks (pw_debug_bounded_wait): one bounded device wait
 // of the forward kernels run against something never released.
 cudaError_t launch_wait_check_decode(int32_t* status, uint32_t polls, cudaStream_t s);

@@ -7,11 +7,18 @@
 // tensor cores:
 //
 //   permute    pairs grouped by expert (offsets, perm)          [pw_route.cu]
-//   gather     xg[pos] = fp16(hidden[perm[pos] / k])            (one pass)
+//   gather     xg[pos] = fp16(hidden[perm[pos] / k] * 2^-e_pos), with the
+//              power of two that puts the row's largest magnitude in [1, 2)
+//              (stored as scale[pos] = 2^e_pos)           (one warp per row)
 //   gate_up    per (expert, 64 gate/up row pairs, 512 tokens):  D = W_gu x^T
-//              in TMEM, epilogue h = SiLU(g) * u -> fp16 h[pos]
+//              in TMEM, epilogue g, u = D * 2^e, h = SiLU(g) * u ->
+//              fp16 h[pos] * 2^-2e
 //   down       per (expert, 128 down rows, 512 tokens, K half): D = W_dn h^T
-//              over one half of K, epilogue y[pair] or y2[pair] (fp32)
+//              over one half of K, epilogue y = D * 2^2e -> y[pair] or
+//              y2[pair] (fp32)
+// The row scales keep every fp16 operand in range for any finite input:
+// |x * 2^-e| < 2, and h * 2^-2e is about (g 2^-e)(u 2^-e), bounded by the
+// weights.
 //   combine    out[t] = sum_j w_tj * (y + y2)[t*k + j], j order (one pass)
 //
 // GEMM kernel: one CTA per SM, persistent, 27 warps in five roles.
@@ -53,8 +60,9 @@
 // barrier group takes the same path even while unwinding.
 //
 // Operand precision: the weights are exact fp16 LUT values; hidden states are
-// converted bf16 -> fp16 (exact for |x| in fp16's normal range, |x| < 65504);
-// h is stored as fp16; all accumulation is fp32.
+// scaled by a power of two per row and converted bf16 -> fp16 (exact unless a
+// value falls below fp16's normal range relative to its row's largest, i.e.
+// below 2^-14 of it); h is stored as fp16 (scaled); all accumulation is fp32.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -128,6 +136,7 @@ struct GemmArgs {
   const pw_block_entry* table;
   const int32_t* offsets;   // [E+1]
   const int32_t* perm;      // [n_pairs]
+  const float* xscale;      // [n_pairs] 2^e of each grouped position's row
   __half* h_ws;             // [n_pairs][I] (gate_up writes, down reads through TMA)
   float* y_ws;              // [n_pairs][H]
   float* y_ws2;             // [n_pairs][H]: the second K half's partial sums (ksplit 2)
@@ -463,6 +472,25 @@ __device__ __forceinline__ void planes_to_index_half(const uint32_t (&P)[Q], uin
   ib[3] = hi1;
 }
 
+// The fp16 weights of chunk cc (8 columns, 8cc .. 8cc + 7) of a row's
+// 16-column half from the half's indices: entry v of the row's LUT at v * 256
+// + slot (fp16).  packed[i] holds columns 8cc + 2i and 8cc + 2i + 1.
+__device__ __forceinline__ void dequant_chunk(const uint32_t (&ib)[4], int cc, uint32_t slot,
+                                              uint32_t (&packed)[4]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t word = ib[2 * cc + h];
+    uint32_t v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t off = __byte_perm(word, slot, 0x6504 | (j << 4));
+      v[j] = *reinterpret_cast<const uint16_t*>(g_psmem + off);
+    }
+    packed[2 * h] = __byte_perm(v[0], v[1], 0x5410);
+    packed[2 * h + 1] = __byte_perm(v[2], v[3], 0x5410);
+  }
+}
+
 // This thread's share of a tile's k-steps: set `set` takes k-steps set,
 // set + 2, ...; `half` picks the 16 columns.
 template <int Q>
@@ -488,18 +516,7 @@ __device__ void dequant_ksteps(const GemmArgs& a, const DqRow& d, int ksteps, ui
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {   // 16-byte chunk 2*half + cc = 8 columns
       uint32_t packed[4];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t word = ib[2 * cc + h];
-        uint32_t v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t off = __byte_perm(word, d.slot, 0x6504 | (j << 4));
-          v[j] = *reinterpret_cast<const uint16_t*>(g_psmem + off);
-        }
-        packed[2 * h] = __byte_perm(v[0], v[1], 0x5410);
-        packed[2 * h + 1] = __byte_perm(v[2], v[3], 0x5410);
-      }
+      dequant_chunk(ib, cc, d.slot, packed);
       const uint32_t c = 2 * half + cc;
       const uint32_t dst = row_base + ((c ^ sw) << 4);
       asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[0]),
@@ -540,11 +557,14 @@ __device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, i
     for (int j = 0; j < 16; ++j) {
       const float send = up ? v[2 * j] : v[2 * j + 1];
       const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
-      const float g = up ? recv : v[2 * j];
-      const float u = up ? v[2 * j + 1] : recv;
-      const float h = __fdividef(g, 1.f + __expf(-g)) * u;
       const int tok = 2 * j + up;
-      st_shared_u16(buf + (tok * 64 + hc) * 2, __half_as_ushort(__float2half_rn(h)));
+      const int n = c * 32 + tok;
+      const float sc = n < ntok ? __ldg(a.xscale + pos0 + n) : 1.f;   // 2^e of the token's row
+      const float isc = 1.f / sc;                                     // exact: a power of two
+      const float g = (up ? recv : v[2 * j]) * sc;
+      const float u = (up ? v[2 * j + 1] : recv) * sc;
+      const float h = g * (1.f / (1.f + __expf(-g))) * u;
+      st_shared_u16(buf + (tok * 64 + hc) * 2, __half_as_ushort(__float2half_rn(h * isc * isc)));
     }
     named_sync_epi_group(group);   // the chunk is staged
 #pragma unroll
@@ -585,7 +605,8 @@ __device__ void epilogue_down(const GemmArgs& a, const Tile& tile, int pos0, int
       const int n = c * 32 + j;
       if (n < ntok) {
         const int pair = a.perm[pos0 + n];
-        y[static_cast<long long>(pair) * a.H + row] = v[j];
+        const float sc = __ldg(a.xscale + pos0 + n);
+        y[static_cast<long long>(pair) * a.H + row] = v[j] * sc * sc;
       }
     }
   }
@@ -860,34 +881,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- gather / combine
 
-// xg[pos][c] = fp16(hidden[perm[pos] / k][c]); positions past the routed
-// pairs are zero.  8 columns per thread.  Also resets the GEMMs' tile counters.
+// xg[pos][c] = fp16(hidden[perm[pos] / k][c] * 2^-e) and scale[pos] = 2^e,
+// e putting the row's largest magnitude in [1, 2) (clamped to [-126, 126]);
+// positions past the routed pairs are zero with scale 1.  One warp per row
+// (two passes over the row: its maximum, then the scaled fp16 values, 8
+// columns per lane and step).  Also resets the GEMMs' tile counters.
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ hidden,
                                                      const int32_t* __restrict__ perm,
                                                      const int32_t* __restrict__ offsets, int E,
                                                      int k, int H, int n_pairs,
                                                      __half* __restrict__ xg,
+                                                     float* __restrict__ xscale,
                                                      int32_t* __restrict__ counters) {
   if (blockIdx.x == 0 && threadIdx.x < 2) counters[threadIdx.x] = 0;
-  const long long per_row = H / 8;
-  const long long total = static_cast<long long>(n_pairs) * per_row;
+  const int lane = threadIdx.x & 31;
   const int valid = offsets[E];
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int pos = static_cast<int>(i / per_row);
-    const int c = static_cast<int>(i % per_row) * 8;
-    uint4 outv = make_uint4(0, 0, 0, 0);
-    if (pos < valid) {
-      const int t = perm[pos] / k;
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(hidden + static_cast<long long>(t) * H + c));
+  const int warps = static_cast<int>(gridDim.x) * (blockDim.x >> 5);
+  for (int pos = static_cast<int>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); pos < n_pairs;
+       pos += warps) {
+    __half* dst = xg + static_cast<long long>(pos) * H;
+    if (pos >= valid) {
+      for (int c = lane * 8; c < H; c += 256) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+      if (lane == 0) xscale[pos] = 1.f;
+      continue;
+    }
+    const uint16_t* src = hidden + static_cast<long long>(perm[pos] / k) * H;
+    uint32_t m = 0;   // bits of |x|: non-negative floats order like their bit patterns
+    for (int c = lane * 8; c < H; c += 256) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src + c));
+      const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m = max(m, max(wv[j] & 0x7FFFu, (wv[j] >> 16) & 0x7FFFu));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    int e = static_cast<int>((m >> 7) & 0xFFu) - 127;   // exponent of the largest bf16 magnitude
+    e = min(max(e, -126), 126);
+    const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    for (int c = lane * 8; c < H; c += 256) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src + c));
       const uint16_t* b = reinterpret_cast<const uint16_t*>(&raw);
       __half2 h[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        h[j] = __floats2half2_rn(bf16_bits_to_float(b[2 * j]), bf16_bits_to_float(b[2 * j + 1]));
-      outv = *reinterpret_cast<const uint4*>(h);
+        h[j] = __floats2half2_rn(bf16_bits_to_float(b[2 * j]) * down, bf16_bits_to_float(b[2 * j + 1]) * down);
+      *reinterpret_cast<uint4*>(dst + c) = *reinterpret_cast<const uint4*>(h);
     }
-    *reinterpret_cast<uint4*>(xg + static_cast<long long>(pos) * H + c) = outv;
+    if (lane == 0) xscale[pos] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
   }
 }
 
@@ -937,6 +977,7 @@ struct WsLayout {
   int32_t* counters;   // [2] tile counters of the two GEMM launches
   int32_t* offsets;
   int32_t* perm;
+  float* xscale;       // [P] 2^e of each gathered row
   __half* xg;
   __half* h;
   float* y;
@@ -953,6 +994,8 @@ WsLayout carve_ws(void* ws, const pw_moe_shape& s) {
   p += round256(sizeof(int32_t) * (s.E + 1));
   w.perm = reinterpret_cast<int32_t*>(p);
   p += round256(sizeof(int32_t) * P);
+  w.xscale = reinterpret_cast<float*>(p);
+  p += round256(sizeof(float) * P);
   w.xg = reinterpret_cast<__half*>(p);
   p += round256(2 * P * s.H);
   w.h = reinterpret_cast<__half*>(p);
@@ -1004,6 +1047,142 @@ cudaError_t configure_gemm() {
 
 }  // namespace
 
+namespace {
+
+// ---------------------------------------------------------------- checks
+//
+// The dequant warps' index extraction and LUT lookups, run on a whole block
+// and written back in column order, for a bit-exact comparison with the
+// format's definition.
+
+// One thread per (row n, word column w): both 16-column halves.
+template <int Q>
+__global__ void __launch_bounds__(256) half_index_check_kernel(const uint32_t* __restrict__ planes,
+                                                               int N, int KW, uint8_t* __restrict__ idx,
+                                                               const BitConsts bc) {
+  const long long total = static_cast<long long>(N) * KW;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long wcol = i / N, n = i % N;
+    uint32_t P[Q];
+#pragma unroll
+    for (int p = 0; p < Q; ++p) P[p] = planes[p * total + wcol * N + n];
+    uint8_t* row = idx + n * (32LL * KW) + 32 * wcol;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t ib[4];
+      planes_to_index_half<Q>(P, half ? 0x7362u : 0x5140u, ib, bc);
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          row[16 * half + 4 * m + j] = static_cast<uint8_t>((ib[m] >> (8 * j)) & 255u);
+    }
+  }
+}
+
+// One CTA of 128 threads per 128 rows, the dequant warps' LUT layout (entry
+// v of a row at v * 256 + slot, four rows per line): each thread loads its
+// row's whole LUT, then dequantises every word column of it.
+template <int Q>
+__global__ void __launch_bounds__(128) half_dequant_check_kernel(const uint32_t* __restrict__ planes,
+                                                                 const uint16_t* __restrict__ lut,
+                                                                 int N, int KW,
+                                                                 float* __restrict__ out,
+                                                                 const BitConsts bc) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t slot = static_cast<uint32_t>((w >> 1) * 128 + lane * 4 + (w & 1) * 2);
+  const long long plane = static_cast<long long>(N) * KW;
+  for (int m0 = blockIdx.x * 128; m0 < N; m0 += gridDim.x * 128) {
+    const int row = m0 + 32 * w + lane;
+    __syncthreads();   // the previous rows' lookups are done
+    if (row < N)
+      for (int part = 0; part < 4; ++part) load_lut<Q>(lut, row, slot, part);
+    __syncthreads();
+    if (row >= N) continue;
+    for (int wcol = 0; wcol < KW; ++wcol) {
+      uint32_t P[Q];
+#pragma unroll
+      for (int p = 0; p < Q; ++p) P[p] = planes[p * plane + static_cast<long long>(wcol) * N + row];
+      float* dst = out + static_cast<long long>(row) * (32LL * KW) + 32 * wcol;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t ib[4];
+        planes_to_index_half<Q>(P, half ? 0x7362u : 0x5140u, ib, bc);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t packed[4];
+          dequant_chunk(ib, cc, slot, packed);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __half2 h2 = *reinterpret_cast<const __half2*>(&packed[i]);
+            dst[16 * half + 8 * cc + 2 * i] = __low2float(h2);
+            dst[16 * half + 8 * cc + 2 * i + 1] = __high2float(h2);
+          }
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_half_index_check(const uint32_t* planes, int N, int K, int q, uint8_t* idx,
+                                    cudaStream_t s) {
+  const BitConsts bc = make_bit_consts();
+  const long long total = static_cast<long long>(N) * (K / 32);
+  const int grid = static_cast<int>(std::min<long long>((total + 255) / 256, 64LL * sm_count()));
+  const int KW = K / 32;
+  switch (q) {
+    case 3: half_index_check_kernel<3><<<grid, 256, 0, s>>>(planes, N, KW, idx, bc); break;
+    case 4: half_index_check_kernel<4><<<grid, 256, 0, s>>>(planes, N, KW, idx, bc); break;
+    case 5: half_index_check_kernel<5><<<grid, 256, 0, s>>>(planes, N, KW, idx, bc); break;
+    case 6: half_index_check_kernel<6><<<grid, 256, 0, s>>>(planes, N, KW, idx, bc); break;
+    case 8: half_index_check_kernel<8><<<grid, 256, 0, s>>>(planes, N, KW, idx, bc); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_half_dequant_check(const uint32_t* planes, const uint16_t* lut, int N, int K,
+                                      int q, float* out, cudaStream_t s) {
+  const BitConsts bc = make_bit_consts();
+  const int KW = K / 32;
+  const int grid = std::min((N + 127) / 128, 2 * sm_count());
+  cudaError_t e = cudaSuccess;
+#define PW_HDQ(QQ)                                                                                \
+  do {                                                                                            \
+    e = cudaFuncSetAttribute(half_dequant_check_kernel<QQ>,                                       \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kLutBytes)); \
+    if (e != cudaSuccess) return e;                                                               \
+    half_dequant_check_kernel<QQ><<<grid, 128, kLutBytes, s>>>(planes, lut, N, KW, out, bc);     \
+  } while (0)
+  switch (q) {
+    case 3: PW_HDQ(3); break;
+    case 4: PW_HDQ(4); break;
+    case 5: PW_HDQ(5); break;
+    case 6: PW_HDQ(6); break;
+    case 8: PW_HDQ(8); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef PW_HDQ
+  return cudaGetLastError();
+}
+
+int prefill_ws_section(const pw_moe_shape& shape, int section, size_t* offset, size_t* bytes) {
+  const size_t P = static_cast<size_t>(shape.T) * shape.k;
+  // offsets from any 256-aligned base
+  char* const base = reinterpret_cast<char*>(static_cast<uintptr_t>(1) << 20);
+  const WsLayout w = carve_ws(base, shape);
+  switch (section) {
+    case 0: *offset = reinterpret_cast<const char*>(w.offsets) - base; *bytes = 4 * (static_cast<size_t>(shape.E) + 1); return 0;
+    case 1: *offset = reinterpret_cast<const char*>(w.perm) - base; *bytes = 4 * P; return 0;
+    case 2: *offset = reinterpret_cast<const char*>(w.xg) - base; *bytes = 2 * P * shape.H; return 0;
+    case 3: *offset = reinterpret_cast<const char*>(w.xscale) - base; *bytes = 4 * P; return 0;
+    default: return -1;
+  }
+}
+
 cudaError_t launch_wait_check_mbar(int32_t* status, uint32_t polls, cudaStream_t s) {
   mbar_wait_check_kernel<<<1, 32, 0, s>>>(status, polls);
   return cudaGetLastError();
@@ -1011,7 +1190,7 @@ cudaError_t launch_wait_check_mbar(int32_t* status, uint32_t polls, cudaStream_t
 
 size_t heavy_scratch_bytes(const pw_moe_shape& s) {
   const size_t P = static_cast<size_t>(s.T) * s.k;
-  return 256 + round256(2 * P * s.H) + round256(2 * P * s.I);
+  return 256 + round256(sizeof(float) * P) + round256(2 * P * s.H) + round256(2 * P * s.I);
 }
 
 // Decode calls with experts that hold many pairs: those experts run through
@@ -1028,13 +1207,14 @@ cudaError_t launch_heavy(const LayerArgs& la, const int32_t* offsets, const int3
   char* p = static_cast<char*>(scratch);
   int32_t* counters = reinterpret_cast<int32_t*>(p);
   p += 256;
+  float* xscale = reinterpret_cast<float*>(p);
+  p += round256(sizeof(float) * P);
   __half* xg = reinterpret_cast<__half*>(p);
   p += round256(2 * P * la.H);
   __half* h = reinterpret_cast<__half*>(p);
-  const long long gwork = static_cast<long long>(n_pairs) * (la.H / 8);
-  const int gblocks = static_cast<int>(std::min<long long>((gwork + 255) / 256, 32LL * sms));
+  const int gblocks = static_cast<int>(std::min<long long>((n_pairs + 7) / 8, 32LL * sms));
   gather_kernel<<<gblocks, 256, 0, stream>>>(la.hidden, perm, offsets, la.E, la.k, la.H, n_pairs, xg,
-                                             counters);
+                                             xscale, counters);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap map_x, map_h;
@@ -1049,6 +1229,7 @@ cudaError_t launch_heavy(const LayerArgs& la, const int32_t* offsets, const int3
   g.table = la.table;
   g.offsets = offsets;
   g.perm = perm;
+  g.xscale = xscale;
   g.h_ws = h;
   g.y_ws = y;
   g.y_ws2 = nullptr;
@@ -1068,7 +1249,8 @@ cudaError_t launch_heavy(const LayerArgs& la, const int32_t* offsets, const int3
 size_t prefill_workspace_bytes(const pw_moe_shape& s) {
   const size_t P = static_cast<size_t>(s.T) * s.k;
   return 256 + round256(sizeof(int32_t) * (s.E + 1)) + round256(sizeof(int32_t) * P) +
-         round256(2 * P * s.H) + round256(2 * P * s.I) + 2 * round256(4 * P * s.H);
+         round256(sizeof(float) * P) + round256(2 * P * s.H) + round256(2 * P * s.I) +
+         2 * round256(4 * P * s.H);
 }
 
 bool prefill_shape_ok(const pw_moe_shape& s) {
@@ -1089,10 +1271,9 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
                                  stream);
   if (e != cudaSuccess) return e;
   if ((e = launch_routing_stats(la, stream)) != cudaSuccess) return e;
-  const long long gwork = static_cast<long long>(n_pairs) * (la.H / 8);
-  const int gblocks = static_cast<int>(std::min<long long>((gwork + 255) / 256, 32LL * sms));
+  const int gblocks = static_cast<int>(std::min<long long>((n_pairs + 7) / 8, 32LL * sms));
   gather_kernel<<<gblocks, 256, 0, stream>>>(la.hidden, w.perm, w.offsets, la.E, la.k, la.H,
-                                             n_pairs, w.xg, w.counters);
+                                             n_pairs, w.xg, w.xscale, w.counters);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   CUtensorMap map_x, map_h;
@@ -1107,6 +1288,7 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   g.table = la.table;
   g.offsets = w.offsets;
   g.perm = w.perm;
+  g.xscale = w.xscale;
   g.h_ws = w.h;
   g.y_ws = w.y;
   g.y_ws2 = w.y2;

@@ -328,6 +328,54 @@ int32_t pw_prefill_min_pairs(const pw_moe_shape* shape);
  * and not thread-safe.  Errors: PW_ERR_INVALID_ARG (exactly one is NULL). */
 int pw_set_timing_events(cudaEvent_t before, cudaEvent_t after);
 
+/* ---- checks of the kernels' own code -----------------------------------------
+ * No counterpart on the PagedWeight pages: these run pieces of the forward
+ * kernels' device code on whole blocks and write the results back in plain
+ * order, so that tests can compare them bit for bit with the format's
+ * definition (PagedWeight, "Core components" 1: a b-bit view reads the top b
+ * planes, idx = code >> (8 - b); the weight is the row's LUT entry).
+ *
+ * Index forms the kernels rebuild indices in: */
+#define PW_INDEX_NIBBLES 0  /* decode kernels, q <= 4 (pair-table lookups)          */
+#define PW_INDEX_BYTES   1  /* decode kernels, q = 5, 6, 8 (any q)                  */
+#define PW_INDEX_HALVES  2  /* tensor-core dequant warps (16-column halves)          */
+
+/* idx[n][k] = the index the kernels' extraction code produces for column k of
+ * row n of a block read at bitwidth q in the given form.
+ *   planes device uint32 [>= q][K/32][N];  idx device uint8 [N][K] (output)
+ * Errors: PW_ERR_INVALID_ARG, PW_ERR_SHAPE (K % 32), PW_ERR_UNSUPPORTED_Q (q
+ * off the ladder; q > 4 with PW_INDEX_NIBBLES). */
+int pw_debug_index(const uint32_t* planes, int32_t N, int32_t K, int32_t q, int32_t form,
+                   uint8_t* idx, cudaStream_t stream);
+
+/* w[n][k] = the weight the kernels' table build and lookup give for column k
+ * of row n at bitwidth q, widened to float: path PW_PATH_DECODE builds the
+ * decode kernels' tables (fp32 tables for q = 5, 6, 8; fp16 pair tables for
+ * q = 3, 4) pass by pass as the kernels do; PW_PATH_PREFILL the dequant
+ * warps' fp16 LUT layout.
+ *   planes device uint32 [>= q][K/32][N];  lut device fp16 [N][2^q] (16-byte
+ *   aligned);  w device float [N][K] (output);  table (may be NULL): its status
+ *   word receives PW_ERR_RANGE for a LUT value a pair table cannot hold
+ * Errors: PW_ERR_INVALID_ARG, PW_ERR_SHAPE (K % 32, N % 32), PW_ERR_UNSUPPORTED_Q. */
+int pw_debug_dequant(const uint32_t* planes, const uint16_t* lut, int32_t N, int32_t K, int32_t q,
+                     int32_t path, float* w, pw_page_table* table, cudaStream_t stream);
+
+/* Byte range [*offset, *offset + *bytes) of a forward call's workspace that
+ * holds, after the call (path PW_PATH_DECODE / PW_PATH_PREFILL):
+ *   section 0: offsets int32 [E+1] of the grouping by expert;
+ *   section 1: perm int32 [T*k], the grouped pair ids;
+ *   section 2: decode: the hidden states in the kernels' fp32 form, float
+ *              [T][H], column c of each group of 32 at 4 (c % 8) + c / 8;
+ *              prefill: the gathered rows, fp16 [T*k][H] (grouped order),
+ *              each scaled by 2^-e of its row;
+ *   section 3: decode: the fp16 records, 80 bytes per (token, group of 32
+ *              columns): 32 fp16 x * 2^-e at 8 (c % 4) + 2 (c / 8) + (c / 4) % 2,
+ *              the floats 2^e of columns 0-15 and 16-31 at bytes 64 and 68;
+ *              prefill: the row scales 2^e, float [T*k].
+ * Errors: PW_ERR_INVALID_ARG (unknown path or section, NULL), shape errors. */
+int pw_debug_workspace_section(const pw_moe_shape* shape, int32_t path, int32_t section,
+                               size_t* offset, size_t* bytes);
+
 /* ---- failure-detection check -------------------------------------------------
  * No counterpart on the PagedWeight pages.  Every device-side wait of the
  * forward kernels is bounded so that a wait that can never end (a producer
@@ -357,9 +405,9 @@ int pw_debug_bounded_wait(pw_page_table* table, int32_t which, int32_t polls,
  * workspace: the scratch lives in one static device array of 8 MiB inside
  * libpw (every GPU that loads the library keeps those 8 MiB until the process
  * exits).  The caller still passes inputs and outputs.
- *   - Shapes whose decode scratch, about 4*T*H + 4*T*k*(I + H + 1) + 88*E
- *     + H/8 bytes (each section rounded up to 256 bytes), exceeds 8 MiB are
- *     rejected with
+ *   - Shapes whose decode scratch, about 6.5*T*H + T*k*(6.5*I + 4*H + 4)
+ *     + 116*E + H/8 bytes (each section rounded up to 256 bytes), exceeds
+ *     8 MiB are rejected with
  *     PW_ERR_WORKSPACE (use pw_moe_forward with a workspace instead), as
  *     are shapes beyond the decode path's limits (PW_ERR_SHAPE).
  *   - The first call on each device looks up the array's device address

@@ -3,6 +3,7 @@ expected outputs (in a spawn process pool for the large layers) and the
 rel-L2 tolerance the layer output is held to."""
 import functools
 import multiprocessing as mp
+import os
 
 import numpy as np
 
@@ -70,8 +71,20 @@ def oracle_out_pool(name, hidden, ids, w, q, seed=0, tokens=None, workers=4):
     routed = sorted(set(int(e) for e in np.unique(ids)))
     chunks = [routed[i::workers] for i in range(workers) if routed[i::workers]]
     ctx = mp.get_context("spawn")
-    with ctx.Pool(len(chunks)) as pool:
-        parts = pool.map(_pool_worker, [(name, seed, hidden, ids, q, c, tokens) for c in chunks])
+    # share the host cores between the workers' BLAS instead of oversubscribing
+    threads = str(max(1, (os.cpu_count() or 1) // len(chunks)))
+    saved = {v: os.environ.get(v) for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS")}
+    for v in saved:
+        os.environ[v] = threads
+    try:
+        with ctx.Pool(len(chunks)) as pool:
+            parts = pool.map(_pool_worker, [(name, seed, hidden, ids, q, c, tokens) for c in chunks])
+    finally:
+        for v, old_v in saved.items():
+            if old_v is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = old_v
     y = {}
     for part in parts:
         y.update(part)

@@ -132,10 +132,12 @@ def test_prefill_rejects_unsupported_shape(pw):
         dl.close()
 
 
-def test_mixtral_prefill_sampled_tokens(pw):
+def test_mixtral_prefill_full_output(pw):
     # full-size Mixtral-shaped prefill (4096 tokens, 8 experts, top-2) through
-    # the automatic path; the oracle computes a sample of tokens (all 8
-    # experts' blocks dequantised in fp64)
+    # the automatic path, checked on every token: the oracle computes all
+    # 4096 outputs (8 experts' blocks dequantised in fp64, a spawn pool), and
+    # the error is held per token, so that no token tile of any expert can
+    # hide inside a pooled norm
     from any_precision_bitplane_gb300.layer import DeviceLayer
     name = "mixtral_prefill"
     layer = host_layer(name)
@@ -145,10 +147,10 @@ def test_mixtral_prefill_sampled_tokens(pw):
         ids, w = oracle_route(tok, 2)
         got, status = _run(pw, dl, tok, ids, w, pw.PATH_AUTO)
         assert status == pw.PW_OK
-        rng = np.random.default_rng(1)
-        sample = sorted(set([0, 1, 4095] + rng.choice(4096, 29, replace=False).tolist()))
-        ref = oracle_out_pool(name, tok.hidden_bf16, ids, w, layer.q, tokens=sample, workers=8)
-        assert rel_l2(got[sample], ref) <= REL_TOL
         assert np.isfinite(got).all()
     finally:
         dl.close()
+    ref = oracle_out_pool(name, tok.hidden_bf16, ids, w, layer.q, workers=8)
+    assert rel_l2(got, ref) <= REL_TOL
+    per_token = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
+    assert per_token.max() <= REL_TOL, (int(per_token.argmax()), float(per_token.max()))
