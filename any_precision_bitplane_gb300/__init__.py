@@ -89,6 +89,7 @@ _SIGNATURES = {
     "pw_debug_index": (_c.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P]),
     "pw_debug_dequant": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "pw_debug_workspace_section": (_c.c_int, [_P, _I32, _I32, _P, _P]),
+    "pw_moe_forward_logits": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _c.c_size_t, _I32, _P]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -307,6 +308,32 @@ def moe_forward(hidden, topk_ids, topk_weights, table, I, E, out=None, workspace
                                      _ptr(workspace), workspace.numel(), int(path),
                                      _stream(stream)), "pw_moe_forward")
     return out
+
+
+def moe_forward_logits(hidden, logits, table, I, E, k, out=None, workspace=None, ids=None,
+                       weights=None, path=PATH_AUTO, stream=None):
+    """The layer fed with router logits [T, E] (float32): the routing runs
+    inside the call.  Returns (out, topk ids int32 [T, k], topk weights
+    float32 [T, k])."""
+    _need_cuda(hidden, logits)
+    T, H = hidden.shape
+    dev = hidden.device
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty((T, k), dtype=torch.float32, device=dev)
+    _need_cuda(out, ids, weights)
+    need = workspace_bytes(T, H, I, E, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    s = MoeShape(T, H, I, E, k)
+    _check(lib().pw_moe_forward_logits(ctypes.byref(s), _ptr(hidden), _ptr(logits), _ptr(ids),
+                                       _ptr(weights), table.handle, _ptr(out), _ptr(workspace),
+                                       workspace.numel(), int(path), _stream(stream)),
+           "pw_moe_forward_logits")
+    return out, ids, weights
 
 
 def moe_forward_noalloc(hidden, topk_ids, topk_weights, table, I, E, out=None, stream=None):

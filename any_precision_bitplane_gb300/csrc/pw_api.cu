@@ -63,7 +63,8 @@ int check_shape(const pw_moe_shape* s) {
 
 int forward_impl(const pw_moe_shape* shape, const void* hidden, const int32_t* topk_ids,
                  const float* topk_weights, const pw_page_table* table, float* out,
-                 void* workspace, size_t workspace_bytes, int32_t path, cudaStream_t stream) {
+                 void* workspace, size_t workspace_bytes, int32_t path, cudaStream_t stream,
+                 const float* logits = nullptr) {
   if (path < PW_PATH_AUTO || path > PW_PATH_PREFILL)
     return fail(PW_ERR_INVALID_ARG, "unknown path %d", path);
   LayerArgs a;
@@ -71,6 +72,14 @@ int forward_impl(const pw_moe_shape* shape, const void* hidden, const int32_t* t
   int rc = check_forward_args(shape, hidden, topk_ids, topk_weights, table, out, &a, &empty);
   if (rc || empty) return rc;
   const pw_moe_shape& s = *shape;
+  if (logits != nullptr) {
+    if (!aligned(logits, 4)) return fail(PW_ERR_INVALID_ARG, "logits must be 4-byte aligned");
+    if (s.E > 1024 || s.k > 32)
+      return fail(PW_ERR_SHAPE, "the fused router needs E <= 1024 and k <= 32");
+    a.logits = logits;
+    a.route_ids = const_cast<int32_t*>(topk_ids);
+    a.route_wts = const_cast<float*>(topk_weights);
+  }
   const long long n_pairs = static_cast<long long>(s.T) * s.k;
   if (path == PW_PATH_AUTO) path = (n_pairs >= prefill_min_pairs(s)) ? PW_PATH_PREFILL : PW_PATH_DECODE;
   size_t need = (path == PW_PATH_DECODE) ? decode_workspace_bytes(s) : prefill_workspace_bytes(s);
@@ -522,6 +531,16 @@ int pw_debug_workspace_section(const pw_moe_shape* shape, int32_t path, int32_t 
   const int r = path == PW_PATH_DECODE ? pw::decode_ws_section(*shape, section, offset, bytes)
                                        : pw::prefill_ws_section(*shape, section, offset, bytes);
   return r == 0 ? PW_OK : fail(PW_ERR_INVALID_ARG, "unknown workspace section %d", section);
+}
+
+int pw_moe_forward_logits(const pw_moe_shape* shape, const void* hidden, const float* logits,
+                          int32_t* topk_ids, float* topk_weights, const pw_page_table* table,
+                          float* out, void* workspace, size_t workspace_bytes, int32_t path,
+                          cudaStream_t stream) {
+  if (logits == nullptr && shape != nullptr && shape->T > 0)
+    return fail(PW_ERR_INVALID_ARG, "logits is NULL");
+  return pw::forward_impl(shape, hidden, topk_ids, topk_weights, table, out, workspace,
+                          workspace_bytes, path, stream, logits);
 }
 
 int32_t pw_prefill_min_pairs(const pw_moe_shape* shape) {

@@ -67,6 +67,7 @@
 
 #include "pw_bits.cuh"
 #include "pw_internal.cuh"
+#include "pw_router.cuh"
 
 namespace pw {
 namespace {
@@ -1131,6 +1132,15 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
   }
   extern __shared__ int psm[];
   const int E = a.E, P = a.T * a.k;
+  if (a.logits != nullptr) {
+    // fused routing: the warps route the tokens into topk_ids / topk_weights
+    // (the caller's buffers, by-products of the call) before the grouping
+    for (int t = warp; t < a.T; t += kPrepWarps)
+      route_token_warp(a.logits + static_cast<long long>(t) * E, E, a.k,
+                       a.route_ids + static_cast<long long>(t) * a.k,
+                       a.route_wts + static_cast<long long>(t) * a.k);
+    __syncthreads();   // the routed ids are visible to the whole CTA
+  }
   int* count = psm;                 // [E]
   int* base = count + E;            // [E]
   int* wcnt = base + E;             // [kPrepWarps][E]

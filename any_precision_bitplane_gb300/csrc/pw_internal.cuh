@@ -68,8 +68,11 @@ cudaError_t launch_unpack_top(const uint32_t* planes, int N, int K, int b, uint8
                               cudaStream_t s);
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids,
                               float* wts, cudaStream_t s);
+// With `logits` (float [n_pairs / k][E]) the routing is fused in front of the
+// grouping: ids (then written, [n_pairs]) and route_wts receive its output.
 cudaError_t launch_permute(const int32_t* ids, int n_pairs, int E, int32_t* offsets,
-                           int32_t* perm, int32_t* inv, int32_t* status, cudaStream_t s);
+                           int32_t* perm, int32_t* inv, int32_t* status, cudaStream_t s,
+                           const float* logits = nullptr, int k = 1, float* route_wts = nullptr);
 
 constexpr int kMaxCommitPerLaunch = 240;  // keeps the parameter block under 4 KB
 struct CommitBatch {
@@ -101,6 +104,12 @@ struct LayerArgs {
   int32_t* status;
   int32_t* stats_counts;         // [E] routing statistics to accumulate, or NULL
   float* stats_mass;             // [E]
+  // Fused routing: with logits (float [T][E]) the launch that groups the
+  // pairs first routes the tokens into route_ids / route_wts (which are then
+  // topk_ids / topk_weights); NULL when the caller routed.
+  const float* logits = nullptr;
+  int32_t* route_ids = nullptr;
+  float* route_wts = nullptr;
 };
 // Routing statistics of one call (pairs per expert, sum of their weights),
 // added to a.stats_counts / a.stats_mass; no-op when they are NULL.

@@ -1268,7 +1268,7 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   if (n_pairs == 0) return cudaSuccess;
   WsLayout w = carve_ws(ws, s);
   cudaError_t e = launch_permute(la.topk_ids, n_pairs, la.E, w.offsets, w.perm, nullptr, la.status,
-                                 stream);
+                                 stream, la.logits, la.k, la.route_wts);
   if (e != cudaSuccess) return e;
   if ((e = launch_routing_stats(la, stream)) != cudaSuccess) return e;
   const int gblocks = static_cast<int>(std::min<long long>((n_pairs + 7) / 8, 32LL * sms));

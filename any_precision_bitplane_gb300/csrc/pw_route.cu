@@ -4,64 +4,22 @@
 #include <climits>
 
 #include "pw_internal.cuh"
+#include "pw_router.cuh"
 
 namespace pw {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-// One warp per token.  Lane l owns experts l, l+32, ... (E <= 1024, so one
-// 32-bit mask per lane marks the experts already taken).  Each of the k rounds
-// is a warp argmax by (logit descending, id ascending); softmax is monotone,
-// so selecting on logits selects on probabilities.  The kept weights are the
-// softmax over the kept logits, which equals the full softmax renormalised.
+// One warp per token (route_token_warp).
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits,
                                                          int T, int E, int k,
                                                          int32_t* __restrict__ ids,
                                                          float* __restrict__ wts) {
-  const int lane = threadIdx.x & 31;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
-  const float* row = logits + static_cast<long long>(t) * E;
-  uint32_t taken = 0;
-  int my_e = -1;
-  float my_v = -INFINITY;
-  for (int r = 0; r < k; ++r) {
-    float best_v = -INFINITY;
-    int best_e = INT_MAX;
-    for (int i = 0, e = lane; e < E; ++i, e += 32) {
-      if ((taken >> i) & 1u) continue;
-      const float v = row[e];
-      if (v > best_v || (v == best_v && e < best_e)) {
-        best_v = v;
-        best_e = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, best_v, off);
-      const int oe = __shfl_xor_sync(kFull, best_e, off);
-      if (ov > best_v || (ov == best_v && oe < best_e)) {
-        best_v = ov;
-        best_e = oe;
-      }
-    }
-    if (best_e == INT_MAX) best_e = -1;  // only NaN logits left
-    if (best_e >= 0 && (best_e & 31) == lane) taken |= 1u << (best_e >> 5);
-    if (lane == r) {
-      my_e = best_e;
-      my_v = best_v;
-    }
-  }
-  const float top = __shfl_sync(kFull, my_v, 0);
-  const float ex = (lane < k && my_e >= 0) ? expf(my_v - top) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-  if (lane < k) {
-    ids[static_cast<long long>(t) * k + lane] = my_e;
-    wts[static_cast<long long>(t) * k + lane] = ex / sum;
-  }
+  route_token_warp(logits + static_cast<long long>(t) * E, E, k, ids + static_cast<long long>(t) * k,
+                   wts + static_cast<long long>(t) * k);
 }
 
 // Single CTA of 32 warps; warp w owns the contiguous run of pairs
@@ -77,13 +35,26 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 constexpr int kPermThreads = 1024;
 constexpr int kPermWarps = kPermThreads / 32;
 
+//
+// With `logits` the routing is fused in front: the warps route the tokens
+// (token t on warp t % 32) into ids / wts, which the rest then reads.
 __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __restrict__ ids,
                                                                int n_pairs, int E,
                                                                int32_t* __restrict__ offsets,
                                                                int32_t* __restrict__ perm,
                                                                int32_t* __restrict__ inv,
-                                                               int32_t* status) {
+                                                               int32_t* status,
+                                                               const float* __restrict__ logits,
+                                                               int k, int32_t* route_ids,
+                                                               float* route_wts) {
   extern __shared__ int smem[];
+  if (logits != nullptr) {
+    const int T = n_pairs / k;
+    for (int t = threadIdx.x >> 5; t < T; t += kPermWarps)
+      route_token_warp(logits + static_cast<long long>(t) * E, E, k,
+                       route_ids + static_cast<long long>(t) * k, route_wts + static_cast<long long>(t) * k);
+    __syncthreads();   // the routed ids are visible to the whole CTA
+  }
   int* s_cnt = smem;                   // [kPermWarps][E]: counts, then running starts
   __shared__ int s_warp_sum[kPermWarps];
   const int tid = threadIdx.x;
@@ -165,14 +136,16 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
 }
 
 cudaError_t launch_permute(const int32_t* ids, int n_pairs, int E, int32_t* offsets,
-                           int32_t* perm, int32_t* inv, int32_t* status, cudaStream_t s) {
+                           int32_t* perm, int32_t* inv, int32_t* status, cudaStream_t s,
+                           const float* logits, int k, float* route_wts) {
   const size_t smem = sizeof(int) * static_cast<size_t>(E) * kPermWarps;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  permute_kernel<<<1, kPermThreads, smem, s>>>(ids, n_pairs, E, offsets, perm, inv, status);
+  permute_kernel<<<1, kPermThreads, smem, s>>>(ids, n_pairs, E, offsets, perm, inv, status, logits, k,
+                                               const_cast<int32_t*>(ids), route_wts);
   return cudaGetLastError();
 }
 

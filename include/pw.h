@@ -313,6 +313,24 @@ int pw_moe_forward_path(const pw_moe_shape* shape, const void* hidden, const int
                         void* workspace, size_t workspace_bytes, int32_t path,
                         cudaStream_t stream);
 
+/* The fused layer fed with router logits (PagedWeight, "Core components" 3:
+ * one fused operation; "Core components" 2: the routing mass the planner
+ * tracks is these weights).  The routing, softmax over the E logits, the top
+ * k experts (ties to the lower id) and the kept probabilities renormalised,
+ * runs inside the launch that groups the pairs (the decode path's prep, the
+ * prefill path's permutation), so the call needs no separate router launch;
+ * its result is written to topk_ids / topk_weights (caller-owned outputs,
+ * also the ids and weights the layer then uses), as pw_route_topk would write
+ * it.  Otherwise the same as pw_moe_forward_path.
+ *   logits       device float [T][E]
+ *   topk_ids     device int32 [T][k] (output)
+ *   topk_weights device float [T][k] (output)
+ * Limits: E <= 1024, k <= 32.  Errors: as pw_moe_forward_path. */
+int pw_moe_forward_logits(const pw_moe_shape* shape, const void* hidden, const float* logits,
+                          int32_t* topk_ids, float* topk_weights, const pw_page_table* table,
+                          float* out, void* workspace, size_t workspace_bytes, int32_t path,
+                          cudaStream_t stream);
+
 /* Token count from which PW_PATH_AUTO takes the prefill path for a shape
  * (T*k pairs >= this value). */
 int32_t pw_prefill_min_pairs(const pw_moe_shape* shape);
