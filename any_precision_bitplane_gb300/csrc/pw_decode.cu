@@ -171,7 +171,8 @@ struct DecodeWs {
   SlotInfo* routed_dn;  // [E] routed experts, down bitwidth descending
   int* ctl;        // [0] routed expert count, [1] gate_up tile counter, [2] down tile counter
   int* arrive;     // [H/32]   per 64-row range: down tiles finished
-  int* gu_done;    // [E]      gate_up tiles finished per expert (released by a fence)
+  int* gu_done;    // [P]      gate_up tiles finished per token group, indexed by the
+                   //          group's first grouped position (released by a fence)
   int heavy_min;   // experts with at least this many pairs are left to the GEMM kernels (0: none)
   int early_next;  // 1: the down grid leaves SM slots free, so it lets the next launch start early
 };
@@ -852,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerA
     }
     if (si.err || si.ne <= 0) {   // (a routed expert always holds a pair)
       if (threadIdx.x == 0) {
-        if (si.err && x == 0) latch_status(a.status, si.err);
+        if (si.err > 0 && x == 0) latch_status(a.status, si.err);   // -1: reported elsewhere
         s.misc[2] = atomicAdd(counter, 1);
       }
       __syncthreads();
@@ -865,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerA
         case 6: gateup_tile<6>(a, w, ex, si, x * kPairsPerTile, s, bc, counter); break;
         default: gateup_tile<8>(a, w, ex, si, x * kPairsPerTile, s, bc, counter); break;
       }
-      if (a.I <= kEarlyDownMaxI) pending = si.e;   // the down tiles wait per expert
+      if (a.I <= kEarlyDownMaxI) pending = si.off;   // the down tiles wait per token group
     }
     // claims only grow, so a tile id that does not advance ends the loop
     const int next = static_cast<int>(gridDim.x) + s.misc[2];
@@ -948,14 +949,14 @@ __device__ void down_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWor
   // them: thread 0 polls (the first poll overlaps the LUT load) and acquires,
   // and the barrier extends that to the CTA
   const bool early = a.I <= kEarlyDownMaxI;
-  const int seen = (early && threadIdx.x == 0) ? load_relaxed(w.gu_done + ex.e) : 0;
+  const int seen = (early && threadIdx.x == 0) ? load_relaxed(w.gu_done + ex.off) : 0;
   {  // the LUT does not depend on h
     PassLut<Q, R> pl;
     pass_lut_fetch<Q, R>(ent.lut, pr, pl);
     pass_lut_store<Q, R, COMPACT>(pl, a.status);
   }
   if (!early) grid_dependency_wait();   // the whole gate_up grid is done
-  else if (threadIdx.x == 0) wait_gate_up(w.gu_done + ex.e, seen, a.I / kPairsPerTile, a.status);
+  else if (threadIdx.x == 0) wait_gate_up(w.gu_done + ex.off, seen, a.I / kPairsPerTile, a.status);
   __syncthreads();
   const int nt0 = min(kTG, ex.ne);
   if (nt0 == 1) down_prime<Q, R, 1>(a, w, ex, ent, pr, 0, nt0);
@@ -1158,8 +1159,8 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
   for (int e = tid; e < E; e += kPrepThreads) {
     count[e] = 0;
     wsum[e] = 0.f;
-    w.gu_done[e] = 0;
   }
+  for (int p = tid; p < P; p += kPrepThreads) w.gu_done[p] = 0;
   for (int i = tid; i < kPrepWarps * E; i += kPrepThreads) wcnt[i] = 0;
   if (tid < 16) (&s_bucket[0][0])[tid] = 0;
   for (int i = tid; i < (a.H + 31) / 32; i += kPrepThreads) w.arrive[i] = 0;
@@ -1209,10 +1210,14 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
   }
   // routed experts by bitwidth class (experts the GEMM kernels take are left out)
   const int heavy_min = w.heavy_min > 0 ? w.heavy_min : INT_MAX;
+  // one slot per (expert, group of up to kTG pairs): an expert's groups are
+  // independent tiles, so that a heavily routed expert spreads over many
+  // CTAs instead of looping over its groups inside each tile
   for (int e = tid; e < E; e += kPrepThreads) {
     if (count[e] > 0 && count[e] < heavy_min) {
-      atomicAdd(&s_bucket[0][q_class(e == tid ? t_gu.q : a.table[2 * e].q)], 1);
-      atomicAdd(&s_bucket[1][q_class(e == tid ? t_dn.q : a.table[2 * e + 1].q)], 1);
+      const int ng = (count[e] + kTG - 1) / kTG;
+      atomicAdd(&s_bucket[0][q_class(e == tid ? t_gu.q : a.table[2 * e].q)], ng);
+      atomicAdd(&s_bucket[1][q_class(e == tid ? t_dn.q : a.table[2 * e + 1].q)], ng);
     }
   }
   __syncthreads();
@@ -1265,29 +1270,35 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const LayerAr
       const pw_block_entry dn = e == tid ? t_dn : a.table[2 * e + 1];
       const bool gu_ok = gu.state == PW_PAGE_GPU && supported_q(gu.q);
       const bool dn_ok = dn.state == PW_PAGE_GPU && supported_q(dn.q);
-      SlotInfo si;
-      si.e = e;
-      si.off = base[e] - count[e];
-      si.ne = count[e];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) si.rows[i] = w.perm[si.off + min(i, si.ne - 1)] / a.k;
-      si.q_other = dn.q;
-      si.q = gu.q;
-      si.planes = gu.planes;
-      si.lut = gu.lut;
-      si.err = gu_ok ? PW_OK
-                     : (gu.state != PW_PAGE_GPU ? PW_ERR_PAGE_NOT_RESIDENT : PW_ERR_UNSUPPORTED_Q);
-      w.routed_gu[atomicAdd(&s_bucket[0][q_class(gu.q)], 1)] = si;
+      const int first = base[e] - count[e];
+      const int gu_err = gu_ok ? PW_OK
+                               : (gu.state != PW_PAGE_GPU ? PW_ERR_PAGE_NOT_RESIDENT : PW_ERR_UNSUPPORTED_Q);
       // down tiles of an expert whose gate_up block cannot run write zeros
       // (their h is not valid); the error was latched by the gate_up tiles
-      si.q = dn.q;
-      si.q_other = gu.q;
-      si.planes = dn.planes;
-      si.lut = dn.lut;
-      si.err = !gu_ok ? -1
-               : dn_ok ? PW_OK
-                       : (dn.state != PW_PAGE_GPU ? PW_ERR_PAGE_NOT_RESIDENT : PW_ERR_UNSUPPORTED_Q);
-      w.routed_dn[atomicAdd(&s_bucket[1][q_class(dn.q)], 1)] = si;
+      const int dn_err = !gu_ok ? -1
+                         : dn_ok ? PW_OK
+                                 : (dn.state != PW_PAGE_GPU ? PW_ERR_PAGE_NOT_RESIDENT : PW_ERR_UNSUPPORTED_Q);
+      for (int g0 = 0; g0 < count[e]; g0 += kTG) {
+        SlotInfo si;
+        si.e = e;
+        si.off = first + g0;
+        si.ne = min(kTG, count[e] - g0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) si.rows[i] = w.perm[si.off + min(i, si.ne - 1)] / a.k;
+        si.q_other = dn.q;
+        si.q = gu.q;
+        si.planes = gu.planes;
+        si.lut = gu.lut;
+        // only the expert's first group reports its error
+        si.err = g0 == 0 ? gu_err : (gu_err ? -1 : PW_OK);
+        w.routed_gu[atomicAdd(&s_bucket[0][q_class(gu.q)], 1)] = si;
+        si.q = dn.q;
+        si.q_other = gu.q;
+        si.planes = dn.planes;
+        si.lut = dn.lut;
+        si.err = g0 == 0 ? dn_err : (dn_err > 0 ? -1 : dn_err);
+        w.routed_dn[atomicAdd(&s_bucket[1][q_class(dn.q)], 1)] = si;
+      }
     }
   }
 }
@@ -1490,6 +1501,14 @@ namespace {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Routed slots of a call: one per (expert, group of up to kTG pairs), so at
+// most the pairs, and at most E + P / kTG.
+size_t max_slots(const pw_moe_shape& s) {
+  const size_t P = static_cast<size_t>(s.T) * s.k;
+  const size_t by_groups = static_cast<size_t>(s.E) + P / kTG;
+  return P < by_groups ? P : by_groups;
+}
+
 struct WsSizes {
   size_t xs, xp, hs, hp, y, offsets, perm, routed, ctl, arrive, gu_done;
 };
@@ -1504,10 +1523,10 @@ WsSizes ws_sizes(const pw_moe_shape& s) {
   z.y = round256(4 * P * s.H);
   z.offsets = round256(4 * (static_cast<size_t>(s.E) + 1));
   z.perm = round256(4 * P);
-  z.routed = round256(sizeof(SlotInfo) * static_cast<size_t>(s.E));
+  z.routed = round256(sizeof(SlotInfo) * max_slots(s));
   z.ctl = 256;
   z.arrive = round256(4 * static_cast<size_t>(s.H / 32));
-  z.gu_done = round256(4 * static_cast<size_t>(s.E));
+  z.gu_done = round256(4 * P);
   return z;
 }
 
@@ -1590,7 +1609,7 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
   const bool heavy = hybrid && hybrid_possible(shape);
   w.heavy_min = heavy ? kHeavyMinTokens : 0;
   // grids: at most one tile per resident CTA (2 per SM)
-  const int slots = a.E < n_pairs ? a.E : n_pairs;
+  const int slots = static_cast<int>(max_slots(shape));
   const int resident = 2 * sms;
   const int gu_tiles = slots * (a.I / kPairsPerTile);
   const int dn_tiles = slots * ((a.H + kDownRows - 1) / kDownRows);
