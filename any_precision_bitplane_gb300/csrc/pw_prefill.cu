@@ -551,6 +551,9 @@ __device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, i
   const uint32_t buf = sbase + kOffStage + group * kStageBuf;
   for (int c = group; c < BN / 32; c += 2) {
     if (c * 32 >= ntok) break;
+    // lane L holds 2^e of the chunk's token L (its load overlaps the TMEM read)
+    const int nl = c * 32 + lane;
+    const float sc_l = nl < ntok ? __ldg(a.xscale + pos0 + nl) : 1.f;
     float v[32];
     tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
 #pragma unroll
@@ -558,12 +561,12 @@ __device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, i
       const float send = up ? v[2 * j] : v[2 * j + 1];
       const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
       const int tok = 2 * j + up;
-      const int n = c * 32 + tok;
-      const float sc = n < ntok ? __ldg(a.xscale + pos0 + n) : 1.f;   // 2^e of the token's row
-      const float isc = 1.f / sc;                                     // exact: a power of two
+      const float sc = __shfl_sync(0xffffffffu, sc_l, tok);
+      // 2^-e from the bits of 2^e (|e| <= 126): exact
+      const float isc = __uint_as_float(0x7F000000u - __float_as_uint(sc));
       const float g = (up ? recv : v[2 * j]) * sc;
       const float u = (up ? v[2 * j + 1] : recv) * sc;
-      const float h = g * (1.f / (1.f + __expf(-g))) * u;
+      const float h = __fdividef(g, 1.f + __expf(-g)) * u;
       st_shared_u16(buf + (tok * 64 + hc) * 2, __half_as_ushort(__float2half_rn(h * isc * isc)));
     }
     named_sync_epi_group(group);   // the chunk is staged
@@ -593,6 +596,14 @@ __device__ void epilogue_down(const GemmArgs& a, const Tile& tile, int pos0, int
   float* const y = tile.kh ? a.y_ws2 : a.y_ws;   // each K part's partial sums
   for (int c = group; c < BN / 32; c += 2) {
     if (c * 32 >= ntok) break;
+    // lane L holds the pair row and 2^e of the chunk's token L
+    const int nl = c * 32 + lane;
+    int pair_l = 0;
+    float sc_l = 1.f;
+    if (nl < ntok) {
+      pair_l = __ldg(a.perm + pos0 + nl);
+      sc_l = __ldg(a.xscale + pos0 + nl);
+    }
     float v[32];
     if (usable) {
       tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
@@ -602,12 +613,10 @@ __device__ void epilogue_down(const GemmArgs& a, const Tile& tile, int pos0, int
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      const int n = c * 32 + j;
-      if (n < ntok) {
-        const int pair = a.perm[pos0 + n];
-        const float sc = __ldg(a.xscale + pos0 + n);
-        y[static_cast<long long>(pair) * a.H + row] = v[j] * sc * sc;
-      }
+      const int pair = __shfl_sync(0xffffffffu, pair_l, j);
+      const float sc = __shfl_sync(0xffffffffu, sc_l, j);
+      // (v 2^e) 2^e: two steps, so that 2^2e itself never has to be finite
+      if (c * 32 + j < ntok) y[static_cast<long long>(pair) * a.H + row] = v[j] * sc * sc;
     }
   }
 }
