@@ -43,7 +43,10 @@
 //               64-byte-swizzled, K-major A stage.
 //   warp 22     allocates the 512 TMEM columns; lane 0 issues per k-step two
 //               K=16 steps of two tcgen05.mma (M=128, N=256 each, fp16 x
-//               fp16 -> fp32) into columns [0,256) and [256,512).
+//               fp16 -> fp32) into columns [0,256) and [256,512).  A stage's
+//               A rows and token rows complete one barrier; the issuer tests
+//               the next stage's barrier inside the same instruction block as
+//               the current MMAs, so the test's latency hides behind them.
 //   warps 16-19 and 23-26: epilogue, two groups of four (TMEM lane quarter =
 //               warp % 4) that take alternate 32-column chunks of the
 //               accumulator, so that it is drained twice as fast (the MMA
@@ -107,15 +110,16 @@ constexpr int kMaxExperts = 1024;
 
 // Shared memory (offsets from the dynamic base, which must be 1024-aligned):
 // the LUT sits at offset 0 so that lookups address the dynamic symbol with a
-// register offset only.
+// register offset only; the plane-word ring, the epilogue buffers, barriers
+// and tile prefix follow; the A/B stages come last.
 constexpr uint32_t kOffLut = 0;
-constexpr uint32_t kOffA = kOffLut + kLutBytes;
-constexpr uint32_t kOffB = kOffA + NST * kAStage;
-constexpr uint32_t kOffPlanes = kOffB + NST * kBStage;
+constexpr uint32_t kOffPlanes = kOffLut + kLutBytes;
 constexpr uint32_t kOffStage = kOffPlanes + NPS * kPlaneStage;
 constexpr uint32_t kOffBar = kOffStage + 2 * kStageBuf;        // 8-byte barriers
-constexpr int kBarFullA = 0, kBarFullB = NST, kBarEmpty = 2 * NST, kBarPlFull = 3 * NST,
-              kBarPlEmpty = 3 * NST + NPS, kBarTileFull = 3 * NST + 2 * NPS,
+// kBarFull[i]: stage i holds its A rows (dequant arrivals) and its token rows
+// (the token producer's arrival with the expected bytes, and the copies).
+constexpr int kBarFull = 0, kBarEmpty = NST, kBarPlFull = 2 * NST,
+              kBarPlEmpty = 2 * NST + NPS, kBarTileFull = 2 * NST + 2 * NPS,
               kBarTileEmpty = kBarTileFull + kTileRing, kBarAccFull = kBarTileEmpty + kTileRing,
               kBarAccEmpty = kBarAccFull + 1, kBarFinal = kBarAccEmpty + 1,
               kNumBars = kBarFinal + 1;
@@ -123,7 +127,9 @@ constexpr int kBarFullA = 0, kBarFullB = NST, kBarEmpty = 2 * NST, kBarPlFull = 
 // tile slots, [8..9] epilogue tile slots, [10] epilogue accumulator flag
 constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;
 constexpr uint32_t kOffPrefix = kOffMisc + 64;                 // tile prefix [E+1]
-constexpr size_t kSmemBytes = kOffPrefix + 4 * (kMaxExperts + 1);
+constexpr uint32_t kOffA = (kOffPrefix + 4 * (kMaxExperts + 1) + 1023) & ~1023u;
+constexpr uint32_t kOffB = kOffA + NST * kAStage;
+constexpr size_t kSmemBytes = kOffB + NST * kBStage;
 static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
 static_assert(kOffB % 1024 == 0 && kOffA % 1024 == 0, "swizzled stages need 1024-byte alignment");
 
@@ -239,14 +245,38 @@ __device__ __forceinline__ uint32_t make_idesc(int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t acc) {
+// One k-step (K = 32: two K = 16 steps) of a tile: the MMAs of token half 0
+// (A x B0 into columns [0, 256)) and, when `two`, of half 1 (A x B1 into
+// [256, 512)), accumulating unless `first`; then their commit to `empty`.
+// With `test`, the barrier `next` is tested (without blocking) for phase
+// `next_par` before the MMAs issue, and the result is returned (1: complete):
+// its latency overlaps the issue instead of preceding the next k-step.
+__device__ __forceinline__ uint32_t issue_kstep(uint32_t tmem, uint64_t a0, uint64_t a1,
+                                                uint64_t b0, uint64_t b1, uint64_t c0, uint64_t c1,
+                                                uint32_t id0, uint32_t id1, bool first, bool two,
+                                                uint32_t empty, uint32_t next, uint32_t next_par,
+                                                bool test) {
+  uint32_t ready;
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      "{\n\t.reg .pred pt, pr, pacc, ptwo, pone;\n\t"
+      "setp.ne.b32 pt, %14, 0;\n\t"
+      "setp.ne.b32 pr, 0, 0;\n\t"
+      "@pt mbarrier.test_wait.parity.shared::cta.b64 pr, [%12], %13;\n\t"
+      "setp.eq.b32 pacc, %10, 0;\n\t"
+      "setp.ne.b32 ptwo, %11, 0;\n\t"
+      "setp.eq.b32 pone, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %3, %5, %8, pacc;\n\t"
+      "@ptwo tcgen05.mma.cta_group::1.kind::f16 [%2], %3, %7, %9, pacc;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %4, %6, %8, pone;\n\t"
+      "@ptwo tcgen05.mma.cta_group::1.kind::f16 [%2], %4, %16, %9, pone;\n\t"
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%15];\n\t"
+      "selp.b32 %0, 1, 0, pr;\n\t}"
+      : "=r"(ready)
+      : "r"(tmem), "r"(tmem + BNH), "l"(a0), "l"(a1), "l"(b0), "l"(b1), "l"(c0), "r"(id0),
+        "r"(id1), "r"(static_cast<uint32_t>(first)), "r"(static_cast<uint32_t>(two)), "r"(next),
+        "r"(next_par), "r"(static_cast<uint32_t>(test)), "r"(empty), "l"(c1)
       : "memory");
+  return ready;
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -524,7 +554,7 @@ __device__ void dequant_ksteps(const GemmArgs& a, const DqRow& d, int ksteps, ui
                    : "memory");
     }
     fence_proxy_async();
-    mbar_arrive(bar_base + 8 * (kBarFullA + st));
+    mbar_arrive(bar_base + 8 * (kBarFull + st));
   }
 }
 
@@ -658,8 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     prefix[a.E] = run;
     for (int i = 0; i < NST; ++i) {
-      mbar_init(bar_base + 8 * (kBarFullA + i), kSetThreads);
-      mbar_init(bar_base + 8 * (kBarFullB + i), 1);
+      mbar_init(bar_base + 8 * (kBarFull + i), kSetThreads + 1);
       mbar_init(bar_base + 8 * (kBarEmpty + i), 1);
     }
     for (int i = 0; i < NPS; ++i) {
@@ -773,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t full = bar_base + 8 * (kBarFullB + stage);
+          const uint32_t full = bar_base + 8 * (kBarFull + stage);
           mbar_arrive_tx(full, halves * kBHalf);
           for (int h = 0; h < halves; ++h)
             tma_load_2d(sbase + kOffB + stage * kBStage + h * kBHalf, &tmap_b, (kr.k0 + s) * BK,
@@ -781,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
       }
-      if (*abort) drain_copies(bar_base, kBarFullB, NST, it, NST);
+      if (*abort) drain_copies(bar_base, kBarFull, NST, it, NST);
     }
   } else if (warp == kPlaneWarp) {
     // ---- plane producer: lane 0 takes tiles and arms the stage barriers;
@@ -844,27 +873,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar_base + 8 * kBarAccEmpty, (acc_it & 1u) ^ 1u, abort, a.status)) break;
         tc_fence_after();
         const int kc = k_range(tile, ksteps, ksplit).kc;
-        bool ok = true;
+        bool ok = true, ready = false;
         for (int s = 0; s < kc; ++s, ++it) {
           const uint32_t stage = it % NST, par = (it / NST) & 1u;
-          if (!mbar_wait(bar_base + 8 * (kBarFullA + stage), par, abort, a.status) ||
-              !mbar_wait(bar_base + 8 * (kBarFullB + stage), par, abort, a.status)) {
+          if (!ready && !mbar_wait(bar_base + 8 * (kBarFull + stage), par, abort, a.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_addr = sbase + kOffA + stage * kAStage;
           const uint32_t b_addr = sbase + kOffB + stage * kBStage;
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-            mma_f16(tmem_base, smem_desc(a_addr + kk * 32), smem_desc(b_addr + kk * 32), id0, acc);
-            if (n1 > 0)
-              mma_f16(tmem_base + BNH, smem_desc(a_addr + kk * 32),
-                      smem_desc(b_addr + kBHalf + kk * 32), id1, acc);
-          }
+          const uint32_t nit = it + 1;
+          // the k-step's MMAs and their commit, with the next stage's barrier
+          // tested in the same breath (its latency hides behind the issue)
+          ready = issue_kstep(tmem_base, smem_desc(a_addr), smem_desc(a_addr + 32),
+                              smem_desc(b_addr), smem_desc(b_addr + 32), smem_desc(b_addr + kBHalf),
+                              smem_desc(b_addr + kBHalf + 32), id0, id1, s == 0, n1 > 0,
+                              bar_base + 8 * (kBarEmpty + stage), bar_base + 8 * (kBarFull + nit % NST),
+                              (nit / NST) & 1u, s + 1 < kc) != 0;
           issued = true;
-          mma_commit(bar_base + 8 * (kBarEmpty + stage));
         }
         if (!ok) break;
         mma_commit(bar_base + 8 * kBarAccFull);
