@@ -993,6 +993,32 @@ __device__ void down_tile(const LayerArgs& a, const DecodeWs& w, const ExpertWor
   }
 }
 
+// out[t][c] = sum_j w_tj * y[t k + j][c] over the token's valid pairs, in j
+// order, for every token t and columns c in [n0, n0 + cols) (cols a multiple
+// of 4): four columns per work item, items i0, i0 + stride, ...
+__device__ void combine_columns(const LayerArgs& a, const DecodeWs& w, int n0, int cols, int i0,
+                                int stride) {
+  const int c4 = cols / 4;
+  const int items = a.T * c4;
+  for (int i = i0; i < items; i += stride) {
+    const int tt = i / c4, c = n0 + 4 * (i - tt * c4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int j = 0; j < a.k; ++j) {
+      const int p = tt * a.k + j;
+      const int e = a.topk_ids[p];
+      if (e < 0 || e >= a.E) continue;
+      const float wt = a.topk_weights[p];
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(w.y + static_cast<long long>(p) * a.H + c));
+      acc.x = fmaf(wt, v.x, acc.x);
+      acc.y = fmaf(wt, v.y, acc.y);
+      acc.z = fmaf(wt, v.z, acc.z);
+      acc.w = fmaf(wt, v.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(a.out + static_cast<long long>(tt) * a.H + c) = acc;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArgs a,
                                                                   const DecodeWs w,
                                                                   const BitConsts bc) {
@@ -1007,19 +1033,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArg
     // every routed expert went to the GEMM kernels (or none was routed):
     // only the combine is left
     grid_dependency_wait();
-    const long long total = static_cast<long long>(a.T) * a.H;
-    for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * kThreads) {
-      const int tt = static_cast<int>(i / a.H), n = static_cast<int>(i % a.H);
-      float acc = 0.f;
-      for (int j = 0; j < a.k; ++j) {
-        const int p = tt * a.k + j;
-        const int e = a.topk_ids[p];
-        if (e < 0 || e >= a.E) continue;
-        acc = fmaf(a.topk_weights[p], __ldcg(w.y + static_cast<long long>(p) * a.H + n), acc);
-      }
-      a.out[i] = acc;
-    }
+    combine_columns(a, w, 0, a.H, static_cast<int>(blockIdx.x) * kThreads + threadIdx.x,
+                    static_cast<int>(gridDim.x) * kThreads);
     return;
   }
   const int tpe = (a.H + kDownRows - 1) / kDownRows;
@@ -1060,17 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArg
     __syncthreads();
     if (s.misc[1]) {
       __threadfence();
-      for (int i = threadIdx.x; i < a.T * rows; i += kThreads) {
-        const int tt = i / rows, n = n0 + i % rows;
-        float acc = 0.f;
-        for (int j = 0; j < a.k; ++j) {
-          const int p = tt * a.k + j;
-          const int e = a.topk_ids[p];
-          if (e < 0 || e >= a.E) continue;
-          acc = fmaf(a.topk_weights[p], __ldcg(w.y + static_cast<long long>(p) * a.H + n), acc);
-        }
-        a.out[static_cast<long long>(tt) * a.H + n] = acc;
-      }
+      combine_columns(a, w, n0, rows, threadIdx.x, kThreads);
     }
     const int next = static_cast<int>(gridDim.x) + s.misc[2];
     t = next > t ? next : total;
