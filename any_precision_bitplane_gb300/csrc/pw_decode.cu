@@ -49,12 +49,12 @@
 //             up in a pair table of the row (2^2q entries, each the fp16
 //             pair {LUT[a], LUT[b]}) with one byte permute and one shared
 //             load per two weights; products are packed fp16 pairs against
-//             fp16 activations, summed in fp16 over the 16 pairs of a word
-//             column and then added to fp32 accumulators with the column
-//             group's power-of-two scale (activations are stored per group
-//             of 32 as x * 2^-e with max |x * 2^-e| in [1, 2), so no fp16
-//             value overflows and the fp16 partial sums keep their relative
-//             precision);
+//             fp16 activations, summed in fp16 over the 8 pairs of each
+//             16-column half of a word column and then added to fp32
+//             accumulators with that half's power-of-two scale (activations
+//             are stored per 16 columns as x * 2^-e with max |x * 2^-e| in
+//             [1, 2), so no fp16 value overflows and the fp16 partial sums
+//             keep their relative precision);
 //   q = 5, 6, 8  byte indices, one lookup per weight in the row's fp32 LUT;
 //             products accumulate as packed fp32 pairs against fp32
 //             activations.

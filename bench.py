@@ -40,7 +40,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
-DECODE_LAUNCHES_PER_CALL = 3   # hidden -> fp32, gate_up + SiLU, down + combine
+DECODE_LAUNCHES_PER_CALL = 3   # prep (grouping, activation forms), gate_up + SiLU, down + combine
+HYBRID_MIN_TOKENS = 16         # calls of this many tokens also launch the heavy experts'
+                               # gather and two GEMM kernels (when the shape suits them)
+
+
+def launches_per_call(cfg, T):
+    """Kernel launches of one decode call of the library (its own kernels only)."""
+    hybrid = (T >= HYBRID_MIN_TOKENS and cfg.H % 128 == 0 and cfg.I % 64 == 0 and cfg.E <= 1024)
+    return DECODE_LAUNCHES_PER_CALL + (3 if hybrid else 0)
 HBM_FALLBACK_GBS = 6800.0
 KERNEL_SOURCES = ("any_precision_bitplane_gb300/csrc/pw_decode.cu",
                   "any_precision_bitplane_gb300/csrc/pw_prefill.cu")
@@ -64,6 +72,16 @@ def parse_args():
     ap.add_argument("--prefill-tokens", type=int, default=0,
                     help="tokens of the prefill section (0: the workload's 4096)")
     return ap.parse_args()
+
+
+SHAPE_NAMES = {"qwen15_decode": "Qwen1.5-MoE-A2.7B-shaped layer",
+               "mixtral_decode": "Mixtral-8x7B-shaped layer",
+               "qwen3_decode": "Qwen3-30B-A3B-shaped layer",
+               "tiny": "tiny layer"}
+
+
+def metric_name(workload):
+    return "MoE-layer tokens/s (decode, %s)" % SHAPE_NAMES.get(workload, workload)
 
 
 def dist_env():
@@ -577,7 +595,7 @@ def native(args):
 
     clocks = sampler.summary(w0, w1)
     line = {
-        "metric": "MoE-layer tokens/s (decode, Qwen1.5-MoE-A2.7B-shaped layer)",
+        "metric": metric_name(cfg.name),
         "value": value,
         "unit": "tokens/s",
         "n_gpus": world,
@@ -607,7 +625,7 @@ def native(args):
                                     "+ combine)",
                           "bytes_per_call": step_bytes},
         "e2e": e2e,
-        "gpu_launches": DECODE_LAUNCHES_PER_CALL * args.steps,
+        "gpu_launches": launches_per_call(cfg, T) * args.steps,
         "clocks": clocks,
     }
     if sweep:
@@ -654,7 +672,7 @@ def reference(args):
     value = (args.steps / k) / dt
     print(json.dumps({
         "impl": "reference",
-        "metric": "MoE-layer tokens/s (decode, Qwen1.5-MoE-A2.7B-shaped layer)",
+        "metric": metric_name(cfg.name),
         "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
