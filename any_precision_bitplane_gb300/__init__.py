@@ -25,6 +25,7 @@ PW_ERR_CUDA = 7
 PW_ERR_TIMEOUT = 8
 PW_ERR_UNSUPPORTED_DEVICE = 9
 PW_ERR_RANGE = 10
+PW_ERR_NOT_BUILT = 11
 
 PW_PAGE_GPU = 0
 PW_PAGE_CPU = 1
@@ -86,6 +87,7 @@ _SIGNATURES = {
     "pw_page_table_commit_after": (_c.c_int, [_P, _I32, _P, _P, _P, _P, _P]),
     "pw_plan_recommit": (_c.c_int, [_I32, _P, _P, _P, _P, _I32, _c.c_int64, _P, _P, _P, _P]),
     "pw_debug_bounded_wait": (_c.c_int, [_P, _I32, _I32, _P]),
+    "pw_debug_gemm_trace": (_c.c_int, [_P, _c.c_size_t, _P]),
     "pw_debug_index": (_c.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P]),
     "pw_debug_dequant": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "pw_debug_workspace_section": (_c.c_int, [_P, _I32, _I32, _P, _P]),
@@ -359,6 +361,25 @@ def debug_bounded_wait(table, which, polls, stream=None):
     limit; it latches PW_ERR_TIMEOUT in the table's status word."""
     _check(lib().pw_debug_bounded_wait(table.handle, int(which), int(polls), _stream(stream)),
            "pw_debug_bounded_wait")
+
+
+TRACE_LIB_PATH = os.path.join(_PKG, "libpw_trace.so")
+
+
+def debug_gemm_trace():
+    """The gate_up GEMM's pipeline trace of the last launch (a library built
+    with build.py --trace): (step uint64 [16, 256, 4], tile uint64 [16, 32, 6],
+    smid uint64 [16]) for CTAs 0, 10, ..., 150; %globaltimer nanoseconds, 0
+    where not reached; smid is the SM id plus one.  Raises PWError
+    (PW_ERR_NOT_BUILT) on a library built without tracing."""
+    import numpy as np
+    need = ctypes.c_size_t(0)
+    lib().pw_debug_gemm_trace(None, 0, ctypes.byref(need))
+    buf = np.zeros(need.value // 8, dtype=np.uint64)
+    _check(lib().pw_debug_gemm_trace(buf.ctypes.data, buf.nbytes, None), "pw_debug_gemm_trace")
+    n_step, n_tile = 16 * 256 * 4, 16 * 32 * 6
+    return (buf[:n_step].reshape(16, 256, 4), buf[n_step:n_step + n_tile].reshape(16, 32, 6),
+            buf[n_step + n_tile:n_step + n_tile + 16])
 
 
 def debug_index(planes, N, K, q, form, idx=None, stream=None):

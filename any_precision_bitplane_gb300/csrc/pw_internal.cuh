@@ -158,5 +158,8 @@ int prefill_ws_section(const pw_moe_shape& shape, int section, size_t* offset, s
 // of the forward kernels run against something never released.
 cudaError_t launch_wait_check_decode(int32_t* status, uint32_t polls, cudaStream_t s);
 cudaError_t launch_wait_check_mbar(int32_t* status, uint32_t polls, cudaStream_t s);
+// The GEMM trace (built with PW_TRACE): false when tracing is compiled out.
+bool gemm_trace_read(void* host, size_t bytes, cudaError_t* err);
+size_t gemm_trace_bytes();
 
 }  // namespace pw

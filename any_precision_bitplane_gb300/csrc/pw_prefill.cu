@@ -43,10 +43,9 @@
 //               64-byte-swizzled, K-major A stage.
 //   warp 22     allocates the 512 TMEM columns; lane 0 issues per k-step two
 //               K=16 steps of two tcgen05.mma (M=128, N=256 each, fp16 x
-//               fp16 -> fp32) into columns [0,256) and [256,512).  A stage's
-//               A rows and token rows complete one barrier; the issuer tests
-//               the next stage's barrier inside the same instruction block as
-//               the current MMAs, so the test's latency hides behind them.
+//               fp16 -> fp32) into columns [0,256) and [256,512), with one
+//               wait per stage: a stage's A rows and token rows complete one
+//               barrier.
 //   warps 16-19 and 23-26: epilogue, two groups of four (TMEM lane quarter =
 //               warp % 4) that take alternate 32-column chunks of the
 //               accumulator, so that it is drained twice as fast (the MMA
@@ -134,6 +133,63 @@ static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
 static_assert(kOffB % 1024 == 0 && kOffA % 1024 == 0, "swizzled stages need 1024-byte alignment");
 
 extern __shared__ __align__(1024) unsigned char g_psmem[];
+
+// ---------------------------------------------------------------- trace
+//
+// Built with -DPW_TRACE (build.py --trace, a separate library), the gate_up
+// GEMM records %globaltimer stamps (ns) of every kTraceStride-th CTA (up to
+// kTraceCtas of them) into a device buffer that pw_debug_gemm_trace copies
+// out: per k-step of the CTA's first kTraceSteps (its ring position), when the
+// MMA issuer found the stage full and when it had issued it, when a dequant
+// set had written it and when the token producer found it empty; per tile
+// (first kTraceTiles), the MMA start (accumulator free) and end (last
+// commit), the epilogue's start and end and the dequant warps' LUT load; and
+// the SM each traced CTA ran on.  The launch path clears the record before
+// each gate_up launch.  Without PW_TRACE every hook is empty.
+constexpr int kTraceSteps = 256, kTraceTiles = 32, kTraceCtas = 16, kTraceStride = 10;
+struct GemmTrace {
+  unsigned long long step[kTraceCtas][kTraceSteps][4];   // ready, issued, dequantised, empty seen
+  unsigned long long tile[kTraceCtas][kTraceTiles][6];   // mma start, mma end, epi start, epi end,
+                                                         // lut start, lut end
+  unsigned long long smid[kTraceCtas];                   // SM id + 1 (0: CTA not traced)
+};
+#ifdef PW_TRACE
+__device__ GemmTrace g_trace;
+__device__ __forceinline__ unsigned long long trace_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ int trace_slot() {
+  const int b = static_cast<int>(blockIdx.x);
+  return (b % kTraceStride == 0 && b / kTraceStride < kTraceCtas) ? b / kTraceStride : -1;
+}
+#define PW_TRACE_STEP(mode, i, k)                                                           \
+  do {                                                                                      \
+    const int ts_ = trace_slot();                                                           \
+    if ((mode) == kGateUp && ts_ >= 0 && (i) < static_cast<uint32_t>(kTraceSteps))           \
+      g_trace.step[ts_][(i)][(k)] = trace_now();                                            \
+  } while (0)
+#define PW_TRACE_TILE(mode, j, k)                                                           \
+  do {                                                                                      \
+    const int ts_ = trace_slot();                                                           \
+    if ((mode) == kGateUp && ts_ >= 0 && (j) < static_cast<uint32_t>(kTraceTiles))           \
+      g_trace.tile[ts_][(j)][(k)] = trace_now();                                            \
+  } while (0)
+#define PW_TRACE_SM(mode)                                                                   \
+  do {                                                                                      \
+    const int ts_ = trace_slot();                                                           \
+    if ((mode) == kGateUp && ts_ >= 0 && threadIdx.x == 0) {                                \
+      unsigned sm_;                                                                         \
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));                                      \
+      g_trace.smid[ts_] = sm_ + 1ull;                                                       \
+    }                                                                                       \
+  } while (0)
+#else
+#define PW_TRACE_STEP(mode, i, k) do { } while (0)
+#define PW_TRACE_TILE(mode, j, k) do { } while (0)
+#define PW_TRACE_SM(mode) do { } while (0)
+#endif
 
 enum Mode { kGateUp = 0, kDown = 1 };
 
@@ -247,36 +303,25 @@ __device__ __forceinline__ uint32_t make_idesc(int n) {
 
 // One k-step (K = 32: two K = 16 steps) of a tile: the MMAs of token half 0
 // (A x B0 into columns [0, 256)) and, when `two`, of half 1 (A x B1 into
-// [256, 512)), accumulating unless `first`; then their commit to `empty`.
-// With `test`, the barrier `next` is tested (without blocking) for phase
-// `next_par` before the MMAs issue, and the result is returned (1: complete):
-// its latency overlaps the issue instead of preceding the next k-step.
-__device__ __forceinline__ uint32_t issue_kstep(uint32_t tmem, uint64_t a0, uint64_t a1,
-                                                uint64_t b0, uint64_t b1, uint64_t c0, uint64_t c1,
-                                                uint32_t id0, uint32_t id1, bool first, bool two,
-                                                uint32_t empty, uint32_t next, uint32_t next_par,
-                                                bool test) {
-  uint32_t ready;
+// [256, 512)), accumulating unless `first`, then their commit to `empty`, in
+// one instruction block.
+__device__ __forceinline__ void issue_kstep(uint32_t tmem, uint64_t a0, uint64_t a1, uint64_t b0,
+                                            uint64_t b1, uint64_t c0, uint64_t c1, uint32_t id0,
+                                            uint32_t id1, bool first, bool two, uint32_t empty) {
   asm volatile(
-      "{\n\t.reg .pred pt, pr, pacc, ptwo, pone;\n\t"
-      "setp.ne.b32 pt, %14, 0;\n\t"
-      "setp.ne.b32 pr, 0, 0;\n\t"
-      "@pt mbarrier.test_wait.parity.shared::cta.b64 pr, [%12], %13;\n\t"
+      "{\n\t.reg .pred pacc, ptwo, pone;\n\t"
       "setp.eq.b32 pacc, %10, 0;\n\t"
       "setp.ne.b32 ptwo, %11, 0;\n\t"
       "setp.eq.b32 pone, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%1], %3, %5, %8, pacc;\n\t"
-      "@ptwo tcgen05.mma.cta_group::1.kind::f16 [%2], %3, %7, %9, pacc;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%1], %4, %6, %8, pone;\n\t"
-      "@ptwo tcgen05.mma.cta_group::1.kind::f16 [%2], %4, %16, %9, pone;\n\t"
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%15];\n\t"
-      "selp.b32 %0, 1, 0, pr;\n\t}"
-      : "=r"(ready)
-      : "r"(tmem), "r"(tmem + BNH), "l"(a0), "l"(a1), "l"(b0), "l"(b1), "l"(c0), "r"(id0),
-        "r"(id1), "r"(static_cast<uint32_t>(first)), "r"(static_cast<uint32_t>(two)), "r"(next),
-        "r"(next_par), "r"(static_cast<uint32_t>(test)), "r"(empty), "l"(c1)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %4, %8, pacc;\n\t"
+      "@ptwo tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %6, %9, pacc;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %5, %8, pone;\n\t"
+      "@ptwo tcgen05.mma.cta_group::1.kind::f16 [%1], %3, %7, %9, pone;\n\t"
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n\t}"
+      ::"r"(tmem), "r"(tmem + BNH), "l"(a0), "l"(a1), "l"(b0), "l"(b1), "l"(c0), "l"(c1),
+        "r"(id0), "r"(id1), "r"(static_cast<uint32_t>(first)), "r"(static_cast<uint32_t>(two)),
+        "r"(empty)
       : "memory");
-  return ready;
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -524,9 +569,9 @@ __device__ __forceinline__ void dequant_chunk(const uint32_t (&ib)[4], int cc, u
 // This thread's share of a tile's k-steps: set `set` takes k-steps set,
 // set + 2, ...; `half` picks the 16 columns.
 template <int Q>
-__device__ void dequant_ksteps(const GemmArgs& a, const DqRow& d, int ksteps, uint32_t it_base,
-                               int set, int half, uint32_t sbase, uint32_t bar_base,
-                               volatile int* abort, const BitConsts& bc) {
+__device__ void dequant_ksteps(const GemmArgs& a, Mode mode, const DqRow& d, int ksteps,
+                               uint32_t it_base, int set, int half, uint32_t sbase,
+                               uint32_t bar_base, volatile int* abort, const BitConsts& bc) {
   const uint32_t sel = half ? 0x7362u : 0x5140u;
   const uint32_t sw = (static_cast<uint32_t>(d.r) >> 1) & 3u;
   for (int ks = set; ks < ksteps; ks += 2) {
@@ -555,7 +600,9 @@ __device__ void dequant_ksteps(const GemmArgs& a, const DqRow& d, int ksteps, ui
     }
     fence_proxy_async();
     mbar_arrive(bar_base + 8 * (kBarFull + st));
+    if ((threadIdx.x & 255) == 0) PW_TRACE_STEP(mode, it, 2);
   }
+  (void)mode;
 }
 
 template <int Q>
@@ -563,9 +610,11 @@ __device__ __forceinline__ void dequant_tile(const GemmArgs& a, Mode mode, const
                                              const DqRow& d, int ksteps, uint32_t it_base, int set,
                                              int half, uint32_t sbase, uint32_t bar_base,
                                              volatile int* abort, const BitConsts& bc) {
+  if (threadIdx.x == 0) PW_TRACE_TILE(mode, it_base / ksteps, 4);
   load_lut<Q>(ent.lut, d.grow, d.slot, 2 * set + half);
   named_sync_dq();
-  dequant_ksteps<Q>(a, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc);
+  if (threadIdx.x == 0) PW_TRACE_TILE(mode, it_base / ksteps, 5);
+  dequant_ksteps<Q>(a, mode, d, ksteps, it_base, set, half, sbase, bar_base, abort, bc);
 }
 
 // ---------------------------------------------------------------- epilogue
@@ -673,6 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // gate_up tiles always take the whole K range (a compile-time 1 here keeps
   // that instantiation free of the split's index arithmetic)
   const int ksplit = (mode == kGateUp) ? 1 : a.ksplit;
+  PW_TRACE_SM(mode);
   if (sbase & 1023u) {   // the swizzled stages need a 1024-byte aligned base
     if (tid == 0) latch_status(a.status, PW_ERR_CUDA);
     return;
@@ -762,8 +812,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mode == kDown) epilogue_down(a, tile, pos0, ntok, false, tmem_base, quarter, lane, group);
         continue;
       }
-      if (tid_e == 0)
+      if (tid_e == 0) {
         *acc_ok = mbar_wait(bar_base + 8 * kBarAccFull, acc_it & 1u, abort, a.status) ? 1 : 0;
+        PW_TRACE_TILE(mode, acc_it, 2);
+      }
       ++acc_it;
       named_sync_epi();
       if (!*acc_ok) break;
@@ -774,6 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         epilogue_down(a, tile, pos0, ntok, true, tmem_base, quarter, lane, group);
       tc_fence_before();
       mbar_arrive(bar_base + 8 * kBarAccEmpty);
+      if (tid_e == 0) PW_TRACE_TILE(mode, acc_it - 1, 3);
     }
   } else if (warp == kSchedWarp) {
     // ---- scheduler + TMA producer for the token operand
@@ -802,6 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          PW_TRACE_STEP(mode, it, 3);
           const uint32_t full = bar_base + 8 * (kBarFull + stage);
           mbar_arrive_tx(full, halves * kBHalf);
           for (int h = 0; h < halves; ++h)
@@ -872,29 +926,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t id0 = make_idesc(n0), id1 = make_idesc(n1 > 0 ? n1 : 16);
         if (!mbar_wait(bar_base + 8 * kBarAccEmpty, (acc_it & 1u) ^ 1u, abort, a.status)) break;
         tc_fence_after();
+        PW_TRACE_TILE(mode, acc_it, 0);
         const int kc = k_range(tile, ksteps, ksplit).kc;
-        bool ok = true, ready = false;
+        bool ok = true;
         for (int s = 0; s < kc; ++s, ++it) {
           const uint32_t stage = it % NST, par = (it / NST) & 1u;
-          if (!ready && !mbar_wait(bar_base + 8 * (kBarFull + stage), par, abort, a.status)) {
+          if (!mbar_wait(bar_base + 8 * (kBarFull + stage), par, abort, a.status)) {
             ok = false;
             break;
           }
+          PW_TRACE_STEP(mode, it, 0);
           tc_fence_after();
           const uint32_t a_addr = sbase + kOffA + stage * kAStage;
           const uint32_t b_addr = sbase + kOffB + stage * kBStage;
-          const uint32_t nit = it + 1;
-          // the k-step's MMAs and their commit, with the next stage's barrier
-          // tested in the same breath (its latency hides behind the issue)
-          ready = issue_kstep(tmem_base, smem_desc(a_addr), smem_desc(a_addr + 32),
-                              smem_desc(b_addr), smem_desc(b_addr + 32), smem_desc(b_addr + kBHalf),
-                              smem_desc(b_addr + kBHalf + 32), id0, id1, s == 0, n1 > 0,
-                              bar_base + 8 * (kBarEmpty + stage), bar_base + 8 * (kBarFull + nit % NST),
-                              (nit / NST) & 1u, s + 1 < kc) != 0;
+          issue_kstep(tmem_base, smem_desc(a_addr), smem_desc(a_addr + 32), smem_desc(b_addr),
+                      smem_desc(b_addr + 32), smem_desc(b_addr + kBHalf),
+                      smem_desc(b_addr + kBHalf + 32), id0, id1, s == 0, n1 > 0,
+                      bar_base + 8 * (kBarEmpty + stage));
           issued = true;
+          PW_TRACE_STEP(mode, it, 1);
         }
         if (!ok) break;
         mma_commit(bar_base + 8 * kBarAccFull);
+        PW_TRACE_TILE(mode, acc_it, 1);
         ++acc_it;
       }
       if (*abort && issued) {
@@ -1219,6 +1273,35 @@ int prefill_ws_section(const pw_moe_shape& shape, int section, size_t* offset, s
   }
 }
 
+// The trace of the last traced launch (zeros if the library was built without
+// PW_TRACE); returns false when tracing is compiled out.
+bool gemm_trace_read(void* host, size_t bytes, cudaError_t* err) {
+#ifdef PW_TRACE
+  *err = cudaMemcpyFromSymbol(host, g_trace, sizeof(GemmTrace) < bytes ? sizeof(GemmTrace) : bytes);
+  return true;
+#else
+  (void)host;
+  (void)bytes;
+  *err = cudaSuccess;
+  return false;
+#endif
+}
+
+size_t gemm_trace_bytes() { return sizeof(GemmTrace); }
+
+// Clears the trace record before a traced launch (nothing without PW_TRACE).
+cudaError_t gemm_trace_clear(cudaStream_t stream) {
+#ifdef PW_TRACE
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_trace);
+  if (e != cudaSuccess) return e;
+  return cudaMemsetAsync(p, 0, sizeof(GemmTrace), stream);
+#else
+  (void)stream;
+  return cudaSuccess;
+#endif
+}
+
 cudaError_t launch_wait_check_mbar(int32_t* status, uint32_t polls, cudaStream_t s) {
   mbar_wait_check_kernel<<<1, 32, 0, s>>>(status, polls);
   return cudaGetLastError();
@@ -1275,6 +1358,7 @@ cudaError_t launch_heavy(const LayerArgs& la, const int32_t* offsets, const int3
   const int grid = sms;
   const BitConsts bc = make_bit_consts();
   g.tile_counter = counters;
+  if ((e = gemm_trace_clear(stream)) != cudaSuccess) return e;
   dq_gemm_kernel<kGateUp><<<grid, kThreads, kSmemBytes, stream>>>(g, map_x, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   g.tile_counter = counters + 1;
@@ -1334,6 +1418,7 @@ cudaError_t launch_prefill(const LayerArgs& la, void* ws, cudaStream_t stream) {
   const int grid = sms;
   const BitConsts bc = make_bit_consts();
   g.tile_counter = w.counters;
+  if ((e = gemm_trace_clear(stream)) != cudaSuccess) return e;
   if ((e = record_timing(g_timing.before, stream)) != cudaSuccess) return e;
   dq_gemm_kernel<kGateUp><<<grid, kThreads, kSmemBytes, stream>>>(g, map_x, bc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

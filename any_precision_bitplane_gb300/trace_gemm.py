@@ -1,0 +1,105 @@
+"""Pipeline trace of the tensor-core gate_up GEMM (a measurement tool).
+
+Needs the traced library: `python any_precision_bitplane_gb300/build.py --trace`
+writes libpw_trace.so (the same sources with -DPW_TRACE).  This tool loads that
+library instead of libpw.so, runs a few forward calls of a workload, and
+summarises the %globaltimer stamps that the last gate_up GEMM launch left for
+its CTAs 0, 10, ..., 150 (pw_debug_gemm_trace), with the SM each one ran on:
+
+  per k-step   the MMA issuer's interval between issued stages; the slack
+               between a dequant set announcing a stage and the issuer finding
+               it full (positive: the stage waited for the issuer);
+  per tile     MMA phase (accumulator free -> last commit), epilogue (drain),
+               the gap the issuer spends waiting for the next accumulator, and
+               the dequant warps' LUT load.
+
+Run from the repository root:
+  python -m any_precision_bitplane_gb300.trace_gemm --workload mixtral_prefill --T 2048
+  python -m any_precision_bitplane_gb300.trace_gemm --workload qwen3_decode --T 64
+"""
+import argparse
+import os
+import sys
+
+import numpy as np
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="mixtral_prefill")
+    ap.add_argument("--T", type=int, default=2048)
+    ap.add_argument("--calls", type=int, default=3)
+    args = ap.parse_args()
+
+    sys.path.insert(0, os.getcwd())
+    import torch
+    import any_precision_bitplane_gb300 as pw
+    from any_precision_bitplane_gb300.layer import DeviceLayer
+    from workloads import configs, gen
+
+    if not os.path.exists(pw.TRACE_LIB_PATH):
+        raise SystemExit("build the traced library first: "
+                         "python any_precision_bitplane_gb300/build.py --trace")
+    pw.LIB_PATH = pw.TRACE_LIB_PATH
+    pw.lib()
+
+    cfg = configs.config_by_name(args.workload)
+    layer = gen.make_layer(cfg, 0)
+    dl = DeviceLayer(layer)
+    tok = gen.make_tokens(layer, args.T)
+    ids, w = pw.route_topk(torch.from_numpy(tok.logits).cuda(), cfg.k)
+    hidden = torch.from_numpy(tok.hidden_bf16.view(np.int16)).cuda()
+    out = torch.empty((args.T, cfg.H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(pw.workspace_bytes(args.T, cfg.H, cfg.I, cfg.E, cfg.k), dtype=torch.uint8,
+                     device="cuda")
+    for _ in range(args.calls):
+        pw.moe_forward(hidden, ids, w, dl.table, cfg.I, cfg.E, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    step, tile, smid = pw.debug_gemm_trace()
+    step = step.astype(np.int64)
+    tile = tile.astype(np.int64)
+    print("workload %s, T=%d: gate_up GEMM stamps of CTAs 0, 10, ..., 150 (ns unless noted)"
+          % (args.workload, args.T))
+    print("%4s %4s %6s %9s %9s %9s %9s %9s %9s %9s" %
+          ("CTA", "SM", "tiles", "kstep_md", "kstep_p90", "slack_md", "mma_us", "epi_us",
+           "idle_us", "lut_us"))
+    agg = {"kstep": [], "slack": [], "mma": [], "epi": [], "idle": [], "lut": []}
+    for c in range(step.shape[0]):
+        if smid[c] == 0:
+            continue
+        s = step[c]
+        done = np.nonzero((s[:, 0] > 0) & (s[:, 1] > 0))[0]
+        t = tile[c]
+        rows = np.nonzero(t[:, 0] > 0)[0]
+        # consecutive k-steps of one tile only (a tile boundary includes the epilogue wait)
+        gaps = [s[i + 1, 1] - s[i, 1] for i in done[:-1] if (i + 1) in set(done)]
+        slack = [s[i, 0] - s[i, 2] for i in done if s[i, 2] > 0]
+        mma = [t[j, 1] - t[j, 0] for j in rows if t[j, 1] > 0]
+        epi = [t[j, 3] - t[j, 2] for j in rows if t[j, 2] > 0 and t[j, 3] > 0]
+        idle = [t[j + 1, 0] - t[j, 1] for j in rows if j + 1 < t.shape[0] and t[j + 1, 0] > 0
+                and t[j, 1] > 0]
+        lut = [t[j, 5] - t[j, 4] for j in rows if t[j, 4] > 0 and t[j, 5] > 0]
+        # drop the k-step gaps that span a tile boundary (they hold the epilogue)
+        if mma:
+            cut = np.median(gaps) * 4 if gaps else 0
+            gaps = [g for g in gaps if g < cut]
+        for k, v in (("kstep", gaps), ("slack", slack), ("mma", mma), ("epi", epi),
+                     ("idle", idle), ("lut", lut)):
+            agg[k] += list(v)
+
+        def md(v, scale=1.0):
+            return "%9.1f" % (np.median(v) / scale) if len(v) else "%9s" % "-"
+        print("%4d %4d %6d %s %s %s %s %s %s %s" % (
+            c * 10, smid[c] - 1, rows.size, md(gaps),
+            ("%9.1f" % np.percentile(gaps, 90)) if gaps else "%9s" % "-", md(slack),
+            md(mma, 1e3), md(epi, 1e3), md(idle, 1e3), md(lut, 1e3)))
+    print("all traced CTAs: k-step interval median %.0f ns; stage ready %.0f ns before the "
+          "issuer reached it (median); tile MMA phase %.1f us, epilogue %.1f us, issuer idle "
+          "between tiles %.1f us, LUT load %.1f us (medians)" % (
+              np.median(agg["kstep"]), np.median(agg["slack"]), np.median(agg["mma"]) / 1e3,
+              np.median(agg["epi"]) / 1e3, np.median(agg["idle"]) / 1e3,
+              np.median(agg["lut"]) / 1e3))
+
+
+if __name__ == "__main__":
+    main()

@@ -69,6 +69,7 @@ extern "C" {
 #define PW_ERR_RANGE             10  /* device: a LUT value outside the range a block
                                         committed at q <= 4 supports (|v| >= 2048 or
                                         not finite); the block is still computed      */
+#define PW_ERR_NOT_BUILT         11  /* this library was built without the facility  */
 
 /* ---- page states of the Weight Page Table ------------------------------ */
 #define PW_PAGE_GPU          0  /* planes and LUT are in device memory        */
@@ -411,6 +412,28 @@ int pw_debug_workspace_section(const pw_moe_shape* shape, int32_t path, int32_t 
  * or 1, polls outside 1..2^20), PW_ERR_UNSUPPORTED_DEVICE, PW_ERR_CUDA. */
 int pw_debug_bounded_wait(pw_page_table* table, int32_t which, int32_t polls,
                           cudaStream_t stream);
+
+/* Pipeline trace of the tensor-core gate_up GEMM, a measurement hook with no
+ * counterpart on the pages.  A library built with tracing (build.py --trace,
+ * which writes libpw_trace.so) records %globaltimer stamps (nanoseconds) in the
+ * gate_up GEMM launches of both the prefill path and the decode path's heavy
+ * experts, for CTAs 0, 10, 20, ... 150 (trace slot = block index / 10); the
+ * record is cleared before each such launch, so it holds the last one.  This
+ * call copies it (synchronously) into host memory laid out as
+ *   uint64 step[16][256][4]: for the CTA's first 256 k-steps (its ring
+ *          position): [0] the MMA issuer found the stage full, [1] it had
+ *          issued the stage's MMAs and commit, [2] a dequant set had written
+ *          and announced the stage's A rows, [3] the token producer found the
+ *          stage empty (0: not reached);
+ *   uint64 tile[16][32][6]: for the CTA's first 32 tiles: [0] MMA start (the
+ *          accumulator free), [1] last commit, [2] epilogue start, [3]
+ *          epilogue end, [4] LUT load start, [5] LUT load end;
+ *   uint64 smid[16]: the SM the CTA ran on, plus one (0: no such CTA).
+ *   host    host buffer of at least *needed bytes
+ *   needed  (may be NULL) receives the record's size
+ * Errors: PW_ERR_INVALID_ARG (NULL or short buffer), PW_ERR_NOT_BUILT (built
+ * without tracing), PW_ERR_UNSUPPORTED_DEVICE, PW_ERR_CUDA. */
+int pw_debug_gemm_trace(void* host, size_t bytes, size_t* needed);
 
 /* ---- the fused layer without a workspace ------------------------------------
  * The PagedWeight pages have no counterpart to this entry point; it is a

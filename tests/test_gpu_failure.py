@@ -65,3 +65,11 @@ def test_bounded_wait_rejects_bad_arguments(pw, dl):
         with pytest.raises(pw.PWError) as ei:
             pw.debug_bounded_wait(dl.table, which, polls)
         assert ei.value.code == pw.PW_ERR_INVALID_ARG
+
+
+def test_gemm_trace_needs_the_traced_build(pw):
+    # libpw.so is built without the GEMM trace: the reader says so and
+    # changes nothing (a traced library, build.py --trace, fills the record)
+    with pytest.raises(pw.PWError) as e:
+        pw.debug_gemm_trace()
+    assert e.value.code == pw.PW_ERR_NOT_BUILT
