@@ -12,7 +12,7 @@
 //              (stored as scale[pos] = 2^e_pos)           (one warp per row)
 //   gate_up    per (expert, 64 gate/up row pairs, 512 tokens):  D = W_gu x^T
 //              in TMEM, epilogue g, u = D * 2^e, h = SiLU(g) * u ->
-//              fp16 h[pos] * 2^-2e
+//              fp16 h[pos] * 2^-2e, computed as Dg * Du * sigma(Dg * 2^e)
 //   down       per (expert, 128 down rows, 512 tokens, K half): D = W_dn h^T
 //              over one half of K, epilogue y = D * 2^2e -> y[pair] or
 //              y2[pair] (fp32)
@@ -641,12 +641,13 @@ __device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, i
       const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
       const int tok = 2 * j + up;
       const float sc = __shfl_sync(0xffffffffu, sc_l, tok);
-      // 2^-e from the bits of 2^e (|e| <= 126): exact
-      const float isc = __uint_as_float(0x7F000000u - __float_as_uint(sc));
-      const float g = (up ? recv : v[2 * j]) * sc;
-      const float u = (up ? v[2 * j + 1] : recv) * sc;
-      const float h = __fdividef(g, 1.f + __expf(-g)) * u;
-      st_shared_u16(buf + (tok * 64 + hc) * 2, __half_as_ushort(__float2half_rn(h * isc * isc)));
+      // with g = gs 2^e and u = us 2^e (gs, us: the accumulators of the
+      // scaled operands), h 2^-2e = gs us sigma(g): one rescale, inside sigma,
+      // and nothing that can overflow (sigma of a huge |g| is 0 or 1)
+      const float gs = up ? recv : v[2 * j];
+      const float us = up ? v[2 * j + 1] : recv;
+      const float sig = __fdividef(1.f, 1.f + __expf(-gs * sc));
+      st_shared_u16(buf + (tok * 64 + hc) * 2, __half_as_ushort(__float2half_rn(gs * us * sig)));
     }
     named_sync_epi_group(group);   // the chunk is staged
 #pragma unroll
