@@ -355,6 +355,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// A 16-column TMEM load (32 lanes x 16 columns of 32 bits), issued without
+// waiting: the registers are written when the load completes.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// Waits for the thread's TMEM loads; naming the registers of the last load as
+// operands keeps every use of them below the wait.
+__device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+
 // Both epilogue groups (tile ids and the accumulator flag).
 __device__ __forceinline__ void named_sync_epi() {
   asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
@@ -628,26 +651,45 @@ __device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, i
   const int up = (lane >> 3) & 1;
   const int hc = 16 * quarter + 8 * (lane >> 4) + (lane & 7);
   const uint32_t buf = sbase + kOffStage + group * kStageBuf;
-  for (int c = group; c < BN / 32; c += 2) {
-    if (c * 32 >= ntok) break;
-    // lane L holds 2^e of the chunk's token L (its load overlaps the TMEM read)
-    const int nl = c * 32 + lane;
-    const float sc_l = nl < ntok ? __ldg(a.xscale + pos0 + nl) : 1.f;
-    float v[32];
-    tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
+  const uint32_t lanes = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+  // The group's chunks c = group, group + 2, ... (32 columns each) go in
+  // halves of 16 columns; each half's TMEM load is issued before the previous
+  // half is processed, and each chunk's scale load one chunk ahead.
+  int c = group;
+  if (c * 32 >= ntok) return;
+  uint32_t ra[16], rb[16];
+  tmem_ld16_issue(lanes + c * 32, ra);
+  float sc_next = c * 32 + lane < ntok ? __ldg(a.xscale + pos0 + c * 32 + lane) : 1.f;
+  tmem_wait16(ra);
+  for (;;) {
+    const float sc_l = sc_next;   // lane L: 2^e of the chunk's token L
+    const int cn = c + 2;
+    const bool more = cn < BN / 32 && cn * 32 < ntok;
+    if (more) sc_next = cn * 32 + lane < ntok ? __ldg(a.xscale + pos0 + cn * 32 + lane) : 1.f;
+    tmem_ld16_issue(lanes + c * 32 + 16, rb);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float send = up ? v[2 * j] : v[2 * j + 1];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
-      const int tok = 2 * j + up;
-      const float sc = __shfl_sync(0xffffffffu, sc_l, tok);
-      // with g = gs 2^e and u = us 2^e (gs, us: the accumulators of the
-      // scaled operands), h 2^-2e = gs us sigma(g): one rescale, inside sigma,
-      // and nothing that can overflow (sigma of a huge |g| is 0 or 1)
-      const float gs = up ? recv : v[2 * j];
-      const float us = up ? v[2 * j + 1] : recv;
-      const float sig = __fdividef(1.f, 1.f + __expf(-gs * sc));
-      st_shared_u16(buf + (tok * 64 + hc) * 2, __half_as_ushort(__float2half_rn(gs * us * sig)));
+    for (int hf = 0; hf < 2; ++hf) {
+      if (hf == 1) {
+        tmem_wait16(rb);
+        if (more) tmem_ld16_issue(lanes + cn * 32, ra);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const uint32_t w0 = hf ? rb[2 * jj] : ra[2 * jj];
+        const uint32_t w1 = hf ? rb[2 * jj + 1] : ra[2 * jj + 1];
+        const float v0 = __uint_as_float(w0), v1 = __uint_as_float(w1);
+        const float send = up ? v0 : v1;
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
+        const int tok = 2 * (8 * hf + jj) + up;
+        const float sc = __shfl_sync(0xffffffffu, sc_l, tok);
+        // with g = gs 2^e and u = us 2^e (gs, us: the accumulators of the
+        // scaled operands), h 2^-2e = gs us sigma(g): one rescale, inside
+        // sigma, and nothing that can overflow (sigma of a huge |g| is 0 or 1)
+        const float gs = up ? recv : v0;
+        const float us = up ? v1 : recv;
+        const float sig = __fdividef(1.f, 1.f + __expf(-gs * sc));
+        st_shared_u16(buf + (tok * 64 + hc) * 2, __half_as_ushort(__float2half_rn(gs * us * sig)));
+      }
     }
     named_sync_epi_group(group);   // the chunk is staged
 #pragma unroll
@@ -664,6 +706,9 @@ __device__ void epilogue_gateup(const GemmArgs& a, const Tile& tile, int pos0, i
       }
     }
     named_sync_epi_group(group);   // the buffer is free for the group's next chunk
+    if (!more) break;
+    tmem_wait16(ra);
+    c = cn;
   }
 }
 
