@@ -29,6 +29,8 @@ def main():
     ap.add_argument("--workload", default="mixtral_prefill")
     ap.add_argument("--T", type=int, default=2048)
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--dump", type=int, default=-1,
+                    help="also print the raw k-step stamps of this trace slot (CTA = 10 x slot)")
     args = ap.parse_args()
 
     sys.path.insert(0, os.getcwd())
@@ -93,6 +95,13 @@ def main():
             c * 10, smid[c] - 1, rows.size, md(gaps),
             ("%9.1f" % np.percentile(gaps, 90)) if gaps else "%9s" % "-", md(slack),
             md(mma, 1e3), md(epi, 1e3), md(idle, 1e3), md(lut, 1e3)))
+    if 0 <= args.dump < step.shape[0] and smid[args.dump]:
+        s = step[args.dump]
+        t0 = s[0, 0]
+        print("raw k-step stamps of CTA %d, ns from its first: issuer found full, issued, "
+              "dequant set announced, token producer found empty" % (args.dump * 10))
+        for i in range(min(48, s.shape[0])):
+            print("%4d %s" % (i, " ".join("%8d" % (v - t0) if v else "       -" for v in s[i])))
     print("all traced CTAs: k-step interval median %.0f ns; stage ready %.0f ns before the "
           "issuer reached it (median); tile MMA phase %.1f us, epilogue %.1f us, issuer idle "
           "between tiles %.1f us, LUT load %.1f us (medians)" % (
