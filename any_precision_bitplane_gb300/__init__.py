@@ -369,17 +369,20 @@ TRACE_LIB_PATH = os.path.join(_PKG, "libpw_trace.so")
 def debug_gemm_trace():
     """The gate_up GEMM's pipeline trace of the last launch (a library built
     with build.py --trace): (step uint64 [16, 256, 4], tile uint64 [16, 32, 6],
-    smid uint64 [16]) for CTAs 0, 10, ..., 150; %globaltimer nanoseconds, 0
-    where not reached; smid is the SM id plus one.  Raises PWError
+    smid uint64 [16], dq uint64 [16, 256, 8, 4]) for CTAs 0, 10, ..., 150;
+    %globaltimer nanoseconds, 0 where not reached; smid is the SM id plus one.  Raises PWError
     (PW_ERR_NOT_BUILT) on a library built without tracing."""
     import numpy as np
     need = ctypes.c_size_t(0)
     lib().pw_debug_gemm_trace(None, 0, ctypes.byref(need))
     buf = np.zeros(need.value // 8, dtype=np.uint64)
     _check(lib().pw_debug_gemm_trace(buf.ctypes.data, buf.nbytes, None), "pw_debug_gemm_trace")
-    n_step, n_tile = 16 * 256 * 4, 16 * 32 * 6
-    return (buf[:n_step].reshape(16, 256, 4), buf[n_step:n_step + n_tile].reshape(16, 32, 6),
-            buf[n_step + n_tile:n_step + n_tile + 16])
+    n_step, n_dq, n_tile = 16 * 256 * 4, 16 * 256 * 8 * 4, 16 * 32 * 6
+    step = buf[:n_step].reshape(16, 256, 4)
+    dq = buf[n_step:n_step + n_dq].reshape(16, 256, 8, 4)
+    tile = buf[n_step + n_dq:n_step + n_dq + n_tile].reshape(16, 32, 6)
+    smid = buf[n_step + n_dq + n_tile:n_step + n_dq + n_tile + 16]
+    return step, tile, smid, dq
 
 
 def debug_index(planes, N, K, q, form, idx=None, stream=None):

@@ -149,6 +149,10 @@ extern __shared__ __align__(1024) unsigned char g_psmem[];
 constexpr int kTraceSteps = 256, kTraceTiles = 32, kTraceCtas = 16, kTraceStride = 10;
 struct GemmTrace {
   unsigned long long step[kTraceCtas][kTraceSteps][4];   // ready, issued, dequantised, empty seen
+  // per k-step and dequant warp of its set (8): the warp's wait for the
+  // stage's release done, its announcement of the stage's A rows done, its
+  // wait for the plane words done, its index transpose done
+  unsigned long long dq[kTraceCtas][kTraceSteps][8][4];
   unsigned long long tile[kTraceCtas][kTraceTiles][6];   // mma start, mma end, epi start, epi end,
                                                          // lut start, lut end
   unsigned long long smid[kTraceCtas];                   // SM id + 1 (0: CTA not traced)
@@ -176,6 +180,25 @@ __device__ __forceinline__ int trace_slot() {
     if ((mode) == kGateUp && ts_ >= 0 && (j) < static_cast<uint32_t>(kTraceTiles))           \
       g_trace.tile[ts_][(j)][(k)] = trace_now();                                            \
   } while (0)
+#define PW_TRACE_DQ(mode, i, k)                                                             \
+  do {                                                                                      \
+    const int ts_ = trace_slot();                                                           \
+    if ((mode) == kGateUp && ts_ >= 0 && (i) < static_cast<uint32_t>(kTraceSteps) &&         \
+        (threadIdx.x & 31) == 0)                                                            \
+      g_trace.dq[ts_][(i)][(threadIdx.x >> 5) & 7][(k)] = trace_now();                      \
+  } while (0)
+__device__ __forceinline__ unsigned long long trace_now_after(uint32_t dep) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t) : "r"(dep));   // waits for dep
+  return t;
+}
+#define PW_TRACE_DQ_AFTER(mode, i, k, dep)                                                  \
+  do {                                                                                      \
+    const int ts_ = trace_slot();                                                           \
+    if ((mode) == kGateUp && ts_ >= 0 && (i) < static_cast<uint32_t>(kTraceSteps) &&         \
+        (threadIdx.x & 31) == 0)                                                            \
+      g_trace.dq[ts_][(i)][(threadIdx.x >> 5) & 7][(k)] = trace_now_after(dep);             \
+  } while (0)
 #define PW_TRACE_SM(mode)                                                                   \
   do {                                                                                      \
     const int ts_ = trace_slot();                                                           \
@@ -189,6 +212,8 @@ __device__ __forceinline__ int trace_slot() {
 #define PW_TRACE_STEP(mode, i, k) do { } while (0)
 #define PW_TRACE_TILE(mode, j, k) do { } while (0)
 #define PW_TRACE_SM(mode) do { } while (0)
+#define PW_TRACE_DQ(mode, i, k) do { } while (0)
+#define PW_TRACE_DQ_AFTER(mode, i, k, dep) do { } while (0)
 #endif
 
 enum Mode { kGateUp = 0, kDown = 1 };
@@ -602,6 +627,7 @@ __device__ void dequant_ksteps(const GemmArgs& a, Mode mode, const DqRow& d, int
     const uint32_t ps = it % NPS, pp = (it / NPS) & 1u;
     const uint32_t st = it % NST, sp = (it / NST) & 1u;
     if (!mbar_wait(bar_base + 8 * (kBarPlFull + ps), pp, abort, a.status)) break;
+    PW_TRACE_DQ(mode, it, 2);
     const uint32_t pbase = kOffPlanes + ps * kPlaneStage + d.word * 4;
     uint32_t wd[Q];
 #pragma unroll
@@ -609,7 +635,9 @@ __device__ void dequant_ksteps(const GemmArgs& a, Mode mode, const DqRow& d, int
     mbar_arrive(bar_base + 8 * (kBarPlEmpty + ps));
     uint32_t ib[4];
     planes_to_index_half<Q>(wd, sel, ib, bc);
+    PW_TRACE_DQ_AFTER(mode, it, 3, ib[0] ^ ib[1] ^ ib[2] ^ ib[3]);   // after the transpose
     if (!mbar_wait(bar_base + 8 * (kBarEmpty + st), sp ^ 1u, abort, a.status)) break;
+    PW_TRACE_DQ(mode, it, 0);
     const uint32_t row_base = sbase + kOffA + st * kAStage + d.r * 64;
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {   // 16-byte chunk 2*half + cc = 8 columns
@@ -624,6 +652,7 @@ __device__ void dequant_ksteps(const GemmArgs& a, Mode mode, const DqRow& d, int
     fence_proxy_async();
     mbar_arrive(bar_base + 8 * (kBarFull + st));
     if ((threadIdx.x & 255) == 0) PW_TRACE_STEP(mode, it, 2);
+    PW_TRACE_DQ(mode, it, 1);
   }
   (void)mode;
 }

@@ -57,7 +57,8 @@ def main():
     for _ in range(args.calls):
         pw.moe_forward(hidden, ids, w, dl.table, cfg.I, cfg.E, out=out, workspace=ws)
     torch.cuda.synchronize()
-    step, tile, smid = pw.debug_gemm_trace()
+    step, tile, smid, dq = pw.debug_gemm_trace()
+    dq = dq.astype(np.int64)
     step = step.astype(np.int64)
     tile = tile.astype(np.int64)
     print("workload %s, T=%d: gate_up GEMM stamps of CTAs 0, 10, ..., 150 (ns unless noted)"
@@ -99,9 +100,17 @@ def main():
         s = step[args.dump]
         t0 = s[0, 0]
         print("raw k-step stamps of CTA %d, ns from its first: issuer found full, issued, "
-              "dequant set announced, token producer found empty" % (args.dump * 10))
+              "dequant set announced (its first warp), token producer found the stage free; "
+              "then over the set's 8 warps (first / last): plane words arrived, transpose done, "
+              "release seen, announced"
+              % (args.dump * 10))
+        d = dq[args.dump]
         for i in range(min(48, s.shape[0])):
-            print("%4d %s" % (i, " ".join("%8d" % (v - t0) if v else "       -" for v in s[i])))
+            cols = [[v for v in d[i, :, k] if v] for k in (2, 3, 0, 1)]
+            extra = " ".join("%8d %8d" % (min(c) - t0, max(c) - t0) for c in cols) \
+                if all(cols) else ""
+            print("%4d %s  %s" % (i, " ".join("%8d" % (v - t0) if v else "       -" for v in s[i]),
+                                  extra))
     print("all traced CTAs: k-step interval median %.0f ns; stage ready %.0f ns before the "
           "issuer reached it (median); tile MMA phase %.1f us, epilogue %.1f us, issuer idle "
           "between tiles %.1f us, LUT load %.1f us (medians)" % (

@@ -428,7 +428,11 @@ int pw_debug_bounded_wait(pw_page_table* table, int32_t which, int32_t polls,
  *   uint64 tile[16][32][6]: for the CTA's first 32 tiles: [0] MMA start (the
  *          accumulator free), [1] last commit, [2] epilogue start, [3]
  *          epilogue end, [4] LUT load start, [5] LUT load end;
- *   uint64 smid[16]: the SM the CTA ran on, plus one (0: no such CTA).
+ *   uint64 smid[16]: the SM the CTA ran on, plus one (0: no such CTA);
+ *   uint64 dq[16][256][8][4]: per k-step and warp of the dequant set that owns
+ *          it: [0] the warp's wait for the stage's release done, [1] its
+ *          announcement of the stage's A rows done, [2] its wait for the
+ *          plane words done, [3] its index transpose done.
  *   host    host buffer of at least *needed bytes
  *   needed  (may be NULL) receives the record's size
  * Errors: PW_ERR_INVALID_ARG (NULL or short buffer), PW_ERR_NOT_BUILT (built
