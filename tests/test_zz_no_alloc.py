@@ -79,3 +79,54 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(pw):
         assert "static scratch" in pw.last_error()
     finally:
         dl.close()
+
+
+def test_noalloc_from_two_host_threads(pw):
+    # the library's host state (the cached scratch address, per-device set-up)
+    # is shared by threads; two threads enqueue no-alloc calls onto one
+    # stream (the documented ordering for the shared scratch), each with its
+    # own tokens, and every result matches the workspace path
+    import threading
+    from any_precision_bitplane_gb300.layer import DeviceLayer
+    layer = host_layer("tiny")
+    dl = DeviceLayer(layer)
+    try:
+        stream = torch.cuda.current_stream()
+        jobs = []
+        for seed_T in (16, 12):
+            tok = gen.make_tokens(layer, seed_T)
+            ids_np, w_np = oracle_route(tok, layer.cfg.k)
+            hidden = torch.from_numpy(tok.hidden_bf16.view(np.int16)).cuda()
+            ids = torch.from_numpy(ids_np).cuda()
+            w = torch.from_numpy(w_np).cuda()
+            ref = pw.moe_forward(hidden, ids, w, dl.table, dl.I, dl.E).cpu().numpy()
+            outs = [torch.full((seed_T, dl.H), float("nan"), dtype=torch.float32, device="cuda")
+                    for _ in range(3)]
+            jobs.append((pw.MoeShape(seed_T, dl.H, dl.I, dl.E, layer.cfg.k), hidden, ids, w, ref,
+                         outs))
+        torch.cuda.synchronize()
+        codes = []
+
+        def run(job):
+            shape, hidden, ids, w, _, outs = job
+            for out in outs:
+                rc = pw.lib().pw_moe_forward_noalloc(
+                    ctypes.byref(shape), ctypes.c_void_p(hidden.data_ptr()),
+                    ctypes.c_void_p(ids.data_ptr()), ctypes.c_void_p(w.data_ptr()),
+                    dl.table.handle, ctypes.c_void_p(out.data_ptr()),
+                    ctypes.c_void_p(stream.cuda_stream))
+                codes.append(rc)
+
+        threads = [threading.Thread(target=run, args=(j,)) for j in jobs]
+        for th in threads:
+            th.start()
+        for th in threads:
+            th.join()
+        torch.cuda.synchronize()
+        assert codes == [pw.PW_OK] * 6
+        for _, _, _, _, ref, outs in jobs:
+            for out in outs:
+                assert rel_l2(out.cpu().numpy(), ref) <= REL_TOL
+        assert dl.table.status() == pw.PW_OK
+    finally:
+        dl.close()
