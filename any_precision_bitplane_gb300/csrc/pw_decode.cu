@@ -164,7 +164,8 @@ struct DecodeWs {
   char* xp;        // [T][H/32] records: hidden states, fp16 form
   float* hs;       // [P][I]   SiLU(g) * u by grouped pair position, fp32 form
   char* hp;        // [P][I/32] records: the same in fp16 form (down blocks at q <= 4)
-  float* y;        // [P][H]   expert output, by pair id
+  float* y;        // [P][H]   expert output, by pair id (with dn_ks = 2: its first K half)
+  float* y2;       // [P][H]   the second K half's partial sums (dn_ks = 2), else unused
   int* offsets;    // [E+1]    expert e owns grouped positions offsets[e] .. offsets[e+1]
   int* perm;       // [P]      grouped position -> pair id
   SlotInfo* routed_gu;  // [E] routed experts, gate_up bitwidth descending
@@ -175,6 +176,7 @@ struct DecodeWs {
                    //          group's first grouped position (released by a fence)
   int heavy_min;   // experts with at least this many pairs are left to the GEMM kernels (0: none)
   int early_next;  // 1: the down grid leaves SM slots free, so it lets the next launch start early
+  int dn_ks;       // K parts per down row range: 1, or 2 (long K in calls with few down tiles)
 };
 
 // Rows streamed by one pass: lane L of row slot g owns row
@@ -635,6 +637,19 @@ __device__ __forceinline__ void warp_range(int KW, int& lo, int& hi) {
   hi = ((warp + 1) * KW) / kWarps;
 }
 
+// This warp's word columns of K part kh of KS (the parts split [0, KW) at KW/KS).
+template <int KS>
+__device__ __forceinline__ void warp_range_part(int KW, int kh, int& lo, int& hi) {
+  if constexpr (KS == 1) {
+    warp_range(KW, lo, hi);
+  } else {
+    const int warp = threadIdx.x >> 5;
+    const int k0 = kh * (KW / KS), kc = (kh == KS - 1) ? KW - k0 : KW / KS;
+    lo = k0 + (warp * kc) / kWarps;
+    hi = k0 + ((warp + 1) * kc) / kWarps;
+  }
+}
+
 
 // Spin bound of the down kernel's wait for an expert's gate_up tiles; the
 // wait backs off with a short sleep, so the bound is well over a second.
@@ -893,27 +908,27 @@ __device__ __forceinline__ void down_xs(const LayerArgs& a, const DecodeWs& w,
   }
 }
 
-template <int Q, int R, int NT>
+template <int Q, int R, int NT, int KS>
 __device__ void down_prime(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
-                           const SlotInfo& ent, const PassRows<R>& pr, int g0, int nt) {
+                           const SlotInfo& ent, const PassRows<R>& pr, int g0, int nt, int kh) {
   const int KW = a.I / 32;
   const long long N = a.H;
   int lo, hi;
-  warp_range(KW, lo, hi);
+  warp_range_part<KS>(KW, kh, lo, hi);
   const char* xs[NT];
   down_xs<Q, NT>(a, w, ex, g0, nt, xs);
   ring_prime<Q, R, NT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt);
 }
 
-template <int Q, int R, bool COMPACT, int NT>
+template <int Q, int R, bool COMPACT, int NT, int KS>
 __device__ void down_group(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
                            const SlotInfo& ent, const PassRows<R>& pr, int g0, int nt,
-                           const SmemPtrs& s, const BitConsts& bc, bool primed) {
+                           const SmemPtrs& s, const BitConsts& bc, bool primed, int kh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int KW = a.I / 32;
   const long long N = a.H;
   int lo, hi;
-  warp_range(KW, lo, hi);
+  warp_range_part<KS>(KW, kh, lo, hi);
   const char* xs[NT];
   down_xs<Q, NT>(a, w, ex, g0, nt, xs);
   float2 acc[R][NT];
@@ -935,15 +950,15 @@ __device__ void down_group(const LayerArgs& a, const DecodeWs& w, const ExpertWo
 #pragma unroll
     for (int ww = 0; ww < kWarps; ++ww) y += s.red[((ww * kTG + tk) * 2 + g) * 32 + lane];
     const int row = seg_base<R>(pr, g, lane >> 4) + (lane & 15);
-    w.y[static_cast<long long>(pair) * a.H + row] = y;
+    ((KS == 2 && kh) ? w.y2 : w.y)[static_cast<long long>(pair) * a.H + row] = y;
   }
   __syncthreads();
 }
 
-template <int Q, int R, bool COMPACT>
+template <int Q, int R, bool COMPACT, int KS>
 __device__ void down_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
                           const SlotInfo& ent, const PassRows<R>& pr, const SmemPtrs& s,
-                          const BitConsts& bc) {
+                          const BitConsts& bc, int kh) {
   __syncthreads();
   // the expert's h rows are complete once all of its gate_up tiles released
   // them: thread 0 polls (the first poll overlaps the LUT load) and acquires,
@@ -959,29 +974,29 @@ __device__ void down_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWor
   else if (threadIdx.x == 0) wait_gate_up(w.gu_done + ex.off, seen, a.I / kPairsPerTile, a.status);
   __syncthreads();
   const int nt0 = min(kTG, ex.ne);
-  if (nt0 == 1) down_prime<Q, R, 1>(a, w, ex, ent, pr, 0, nt0);
-  else down_prime<Q, R, kTG>(a, w, ex, ent, pr, 0, nt0);
+  if (nt0 == 1) down_prime<Q, R, 1, KS>(a, w, ex, ent, pr, 0, nt0, kh);
+  else down_prime<Q, R, kTG, KS>(a, w, ex, ent, pr, 0, nt0, kh);
   for (int g0 = 0; g0 < ex.ne; g0 += kTG) {
     const int nt = min(kTG, ex.ne - g0);
     const bool primed = (g0 == 0);
-    if (nt == 1) down_group<Q, R, COMPACT, 1>(a, w, ex, ent, pr, g0, nt, s, bc, primed);
-    else down_group<Q, R, COMPACT, kTG>(a, w, ex, ent, pr, g0, nt, s, bc, primed);
+    if (nt == 1) down_group<Q, R, COMPACT, 1, KS>(a, w, ex, ent, pr, g0, nt, s, bc, primed, kh);
+    else down_group<Q, R, COMPACT, kTG, KS>(a, w, ex, ent, pr, g0, nt, s, bc, primed, kh);
   }
 }
 
 // A down tile of `rows` (64, or 32 on a ragged last tile) rows from n0.
-template <int Q>
+template <int Q, int KS>
 __device__ void down_tile(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
                           const SlotInfo& ent, int n0, int rows, const SmemPtrs& s,
-                          const BitConsts& bc) {
+                          const BitConsts& bc, int kh) {
   if (compact_q<Q>() || rows == 32) {
 #pragma unroll 1
     for (int grp = 0; grp < rows / 32; ++grp) {
       PassRows<1> pr;
       pr.seg[0][0] = n0 + 32 * grp;
       pr.seg[0][1] = n0 + 32 * grp + 16;
-      if constexpr (compact_q<Q>()) down_pass<Q, 1, true>(a, w, ex, ent, pr, s, bc);
-      else down_pass<Q, 1, false>(a, w, ex, ent, pr, s, bc);
+      if constexpr (compact_q<Q>()) down_pass<Q, 1, true, KS>(a, w, ex, ent, pr, s, bc, kh);
+      else down_pass<Q, 1, false, KS>(a, w, ex, ent, pr, s, bc, kh);
     }
   } else {
     PassRows<2> pr;
@@ -989,13 +1004,14 @@ __device__ void down_tile(const LayerArgs& a, const DecodeWs& w, const ExpertWor
     pr.seg[0][1] = n0 + 16;
     pr.seg[1][0] = n0 + 32;
     pr.seg[1][1] = n0 + 48;
-    down_pass<Q, 2, false>(a, w, ex, ent, pr, s, bc);
+    down_pass<Q, 2, false, KS>(a, w, ex, ent, pr, s, bc, kh);
   }
 }
 
 // out[t][c] = sum_j w_tj * y[t k + j][c] over the token's valid pairs, in j
 // order, for every token t and columns c in [n0, n0 + cols) (cols a multiple
 // of 4): four columns per work item, items i0, i0 + stride, ...
+template <int KS>
 __device__ void combine_columns(const LayerArgs& a, const DecodeWs& w, int n0, int cols, int i0,
                                 int stride) {
   const int c4 = cols / 4;
@@ -1009,7 +1025,15 @@ __device__ void combine_columns(const LayerArgs& a, const DecodeWs& w, int n0, i
       const int e = a.topk_ids[p];
       if (e < 0 || e >= a.E) continue;
       const float wt = a.topk_weights[p];
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(w.y + static_cast<long long>(p) * a.H + c));
+      float4 v = __ldcg(reinterpret_cast<const float4*>(w.y + static_cast<long long>(p) * a.H + c));
+      if constexpr (KS == 2) {   // the down tiles' second K half
+        const float4 v2 =
+            __ldcg(reinterpret_cast<const float4*>(w.y2 + static_cast<long long>(p) * a.H + c));
+        v.x += v2.x;
+        v.y += v2.y;
+        v.z += v2.z;
+        v.w += v2.w;
+      }
       acc.x = fmaf(wt, v.x, acc.x);
       acc.y = fmaf(wt, v.y, acc.y);
       acc.z = fmaf(wt, v.z, acc.z);
@@ -1019,6 +1043,9 @@ __device__ void combine_columns(const LayerArgs& a, const DecodeWs& w, int n0, i
   }
 }
 
+// KS: K parts per 64-row range (1, or 2 for long down blocks in calls with
+// few down tiles; the second part's partial sums go to y2).
+template <int KS>
 __global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArgs a,
                                                                   const DecodeWs w,
                                                                   const BitConsts bc) {
@@ -1033,32 +1060,37 @@ __global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArg
     // every routed expert went to the GEMM kernels (or none was routed):
     // only the combine is left
     grid_dependency_wait();
-    combine_columns(a, w, 0, a.H, static_cast<int>(blockIdx.x) * kThreads + threadIdx.x,
-                    static_cast<int>(gridDim.x) * kThreads);
+    combine_columns<1>(a, w, 0, a.H, static_cast<int>(blockIdx.x) * kThreads + threadIdx.x,
+                       static_cast<int>(gridDim.x) * kThreads);
     return;
   }
   const int tpe = (a.H + kDownRows - 1) / kDownRows;
-  const int total = n_routed * tpe;
+  // a tile is (slot, 64-row range, K part); the K parts of a range are
+  // neighbouring tiles
+  constexpr int ks = KS;
+  const int total = n_routed * tpe * ks;
   // A CTA's first tile is its block index; each tile claims the next one
   // from the counter (offset by the grid size) together with its arrival.
   for (int t = blockIdx.x; t < total;) {
-    const int slot = t / tpe, x = t - slot * tpe;
+    const int slot = t / (tpe * ks), rem = t - slot * (tpe * ks);
+    const int x = rem / ks, kh = rem - x * ks;
     const SlotInfo si = w.routed_dn[slot];
     const ExpertWork ex{si.e, si.off, si.ne};
     const int n0 = x * kDownRows;
     const int rows = min(kDownRows, a.H - n0);   // 64, or 32 on a ragged last range
     if (si.err) {
       // this expert contributes zero; gate_up skipped it (h is not valid)
-      if (x == 0 && threadIdx.x == 0 && si.err > 0) latch_status(a.status, si.err);
+      if (x == 0 && kh == 0 && threadIdx.x == 0 && si.err > 0) latch_status(a.status, si.err);
+      float* const yk = (KS == 2 && kh) ? w.y2 : w.y;
       for (int i = threadIdx.x; i < ex.ne * rows; i += kThreads)
-        w.y[static_cast<long long>(w.perm[ex.off + i / rows]) * a.H + n0 + (i % rows)] = 0.f;
+        yk[static_cast<long long>(w.perm[ex.off + i / rows]) * a.H + n0 + (i % rows)] = 0.f;
     } else {
       switch (si.q) {
-        case 3: down_tile<3>(a, w, ex, si, n0, rows, s, bc); break;
-        case 4: down_tile<4>(a, w, ex, si, n0, rows, s, bc); break;
-        case 5: down_tile<5>(a, w, ex, si, n0, rows, s, bc); break;
-        case 6: down_tile<6>(a, w, ex, si, n0, rows, s, bc); break;
-        default: down_tile<8>(a, w, ex, si, n0, rows, s, bc); break;
+        case 3: down_tile<3, KS>(a, w, ex, si, n0, rows, s, bc, kh); break;
+        case 4: down_tile<4, KS>(a, w, ex, si, n0, rows, s, bc, kh); break;
+        case 5: down_tile<5, KS>(a, w, ex, si, n0, rows, s, bc, kh); break;
+        case 6: down_tile<6, KS>(a, w, ex, si, n0, rows, s, bc, kh); break;
+        default: down_tile<8, KS>(a, w, ex, si, n0, rows, s, bc, kh); break;
       }
     }
     // Arrival: the last routed expert to finish this row range combines it.
@@ -1069,13 +1101,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_down_kernel(const LayerArg
       __threadfence();
       const int arrived = atomicAdd(&w.arrive[x], 1);
       const int claim = atomicAdd(&w.ctl[2], 1);
-      s.misc[1] = (arrived == n_routed - 1);
+      s.misc[1] = (arrived == n_routed * ks - 1);
       s.misc[2] = claim;
     }
     __syncthreads();
     if (s.misc[1]) {
       __threadfence();
-      combine_columns(a, w, n0, rows, threadIdx.x, kThreads);
+      combine_columns<KS>(a, w, n0, rows, threadIdx.x, kThreads);
     }
     const int next = static_cast<int>(gridDim.x) + s.misc[2];
     t = next > t ? next : total;
@@ -1322,7 +1354,10 @@ cudaError_t configure_decode() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(decode_down_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_down_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(kSmemBytes));
 }
 }  // namespace
@@ -1514,8 +1549,13 @@ size_t max_slots(const pw_moe_shape& s) {
   return P < by_groups ? P : by_groups;
 }
 
+// Down blocks with at least this many word columns (K = I >= 8192) may split
+// each row range's K over two tiles (calls whose down tiles fill fewer than
+// two rounds of the grid), the second half's partial sums in y2.
+constexpr int kSplitDownMinKW = 256;
+
 struct WsSizes {
-  size_t xs, xp, hs, hp, y, offsets, perm, routed, ctl, arrive, gu_done;
+  size_t xs, xp, hs, hp, y, offsets, perm, routed, ctl, arrive, gu_done, y2;
 };
 
 WsSizes ws_sizes(const pw_moe_shape& s) {
@@ -1532,6 +1572,7 @@ WsSizes ws_sizes(const pw_moe_shape& s) {
   z.ctl = 256;
   z.arrive = round256(4 * static_cast<size_t>(s.H / 32));
   z.gu_done = round256(4 * P);
+  z.y2 = (s.I / 32 >= kSplitDownMinKW) ? round256(4 * P * s.H) : 0;
   return z;
 }
 
@@ -1585,7 +1626,7 @@ int decode_ws_section(const pw_moe_shape& shape, int section, size_t* offset, si
 size_t decode_workspace_bytes(const pw_moe_shape& s, bool hybrid) {
   const WsSizes z = ws_sizes(s);
   const size_t base = z.xs + z.xp + z.hs + z.hp + z.y + z.offsets + z.perm + 2 * z.routed + z.ctl +
-                      z.arrive + z.gu_done;
+                      z.arrive + z.gu_done + z.y2;
   return base + ((hybrid && hybrid_possible(s)) ? heavy_scratch_bytes(s) : 0);
 }
 
@@ -1611,13 +1652,17 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
   w.ctl = reinterpret_cast<int*>(p); p += z.ctl;
   w.arrive = reinterpret_cast<int*>(p); p += z.arrive;
   w.gu_done = reinterpret_cast<int*>(p); p += z.gu_done;
+  w.y2 = z.y2 ? reinterpret_cast<float*>(p) : nullptr; p += z.y2;
   const bool heavy = hybrid && hybrid_possible(shape);
   w.heavy_min = heavy ? kHeavyMinTokens : 0;
   // grids: at most one tile per resident CTA (2 per SM)
   const int slots = static_cast<int>(max_slots(shape));
   const int resident = 2 * sms;
   const int gu_tiles = slots * (a.I / kPairsPerTile);
-  const int dn_tiles = slots * ((a.H + kDownRows - 1) / kDownRows);
+  // long down blocks in calls with few down tiles split each range's K in two
+  // (not with the GEMM kernels, whose rows of y have no second half)
+  w.dn_ks = (!heavy && z.y2 && slots * ((a.H + kDownRows - 1) / kDownRows) < 2 * resident) ? 2 : 1;
+  const int dn_tiles = slots * ((a.H + kDownRows - 1) / kDownRows) * w.dn_ks;
 
   const size_t prep_smem = sizeof(int) * static_cast<size_t>(a.E) * (3 + kPrepWarps);
   if (prep_smem > 48 * 1024) {
@@ -1655,8 +1700,12 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
                        dim3(kThreads), kSmemBytes, stream, a, w, bc);
   if (e != cudaSuccess) return e;
   if ((e = record_timing(g_timing.after, stream)) != cudaSuccess) return e;
-  return launch_dependent(decode_down_kernel, dim3(dn_tiles < resident ? dn_tiles : resident),
-                          dim3(kThreads), kSmemBytes, stream, a, w, bc);
+  const dim3 dn_grid(dn_tiles < resident ? dn_tiles : resident);
+  if (w.dn_ks == 2)
+    return launch_dependent(decode_down_kernel<2>, dn_grid, dim3(kThreads), kSmemBytes, stream,
+                            a, w, bc);
+  return launch_dependent(decode_down_kernel<1>, dn_grid, dim3(kThreads), kSmemBytes, stream, a,
+                          w, bc);
 }
 
 }  // namespace pw

@@ -451,7 +451,8 @@ int pw_debug_gemm_trace(void* host, size_t bytes, size_t* needed);
  * libpw (every GPU that loads the library keeps those 8 MiB until the process
  * exits).  The caller still passes inputs and outputs.
  *   - Shapes whose decode scratch, about 6.5*T*H + T*k*(6.5*I + 4*H + 4)
- *     + 116*E + H/8 bytes (each section rounded up to 256 bytes), exceeds
+ *     + 116*E + H/8 bytes, plus 4*T*k*H when I >= 8192 (each section
+ *     rounded up to 256 bytes), exceeds
  *     8 MiB are rejected with
  *     PW_ERR_WORKSPACE (use pw_moe_forward with a workspace instead), as
  *     are shapes beyond the decode path's limits (PW_ERR_SHAPE).

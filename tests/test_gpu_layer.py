@@ -73,6 +73,10 @@ CUSTOM = [
     ("wideH", 160, 64, 4, 2, 9),
     ("allexp", 256, 512, 8, 8, 3),
     ("manytok", 96, 160, 2, 1, 37),
+    # long down blocks (I >= 8192): the down tiles split K in two parts; 257
+    # words split 128/129 and raggedly over the warps, H = 96 leaves a
+    # 32-row last range
+    ("ksplit", 96, 8224, 3, 2, 3),
 ]
 
 
@@ -88,6 +92,14 @@ def test_uniform_bitwidth(pw, q):
     layer = gen.make_layer(configs.custom("uq", 256, 192, 6, 2, 12), seed=22)
     layer = dataclasses.replace(layer, q=np.full_like(layer.q, q))
     check(pw, layer, "uq%d" % q, 12)
+
+
+@pytest.mark.parametrize("q", [3, 4, 5, 6, 8])
+def test_ksplit_uniform_bitwidth(pw, q):
+    # every table form of the down tiles with K split in two parts
+    layer = gen.make_layer(configs.custom("ksq", 96, 8224, 3, 2, 3), seed=24)
+    layer = dataclasses.replace(layer, q=np.full_like(layer.q, q))
+    check(pw, layer, "ksq%d" % q, 3)
 
 
 @pytest.mark.parametrize("T", [1, 4, 8])
@@ -126,6 +138,18 @@ def test_fused_mixed_launch_equals_sum_of_single_expert_calls(pw):
         total += part
     assert rel_l2(fused, total) <= 1e-5
     assert len(set(int(v) for v in layer.q.ravel())) > 1   # the launch really mixed bitwidths
+
+
+def test_ksplit_forward_is_repeatable(pw):
+    # the two K parts' partial sums are added in a fixed order by the combine
+    layer = gen.make_layer(configs.custom("ksplit_rep", 96, 8224, 3, 2, 3), seed=23)
+    dl = device_layer(layer, "ksplit_rep")
+    tok = gen.make_tokens(layer, 3)
+    ids, w = oracle_route(tok, layer.cfg.k)
+    a, sa = run(pw, dl, tok.hidden_bf16, ids, w)
+    b, sb = run(pw, dl, tok.hidden_bf16, ids, w)
+    assert sa == sb == pw.PW_OK
+    np.testing.assert_array_equal(a, b)
 
 
 def test_forward_is_repeatable(pw):
