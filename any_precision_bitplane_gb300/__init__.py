@@ -88,6 +88,7 @@ _SIGNATURES = {
     "pw_plan_recommit": (_c.c_int, [_I32, _P, _P, _P, _P, _I32, _c.c_int64, _P, _P, _P, _P]),
     "pw_debug_bounded_wait": (_c.c_int, [_P, _I32, _I32, _P]),
     "pw_debug_gemm_trace": (_c.c_int, [_P, _c.c_size_t, _P]),
+    "pw_debug_decode_trace": (_c.c_int, [_P, _c.c_size_t, _P]),
     "pw_debug_index": (_c.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P]),
     "pw_debug_dequant": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "pw_debug_workspace_section": (_c.c_int, [_P, _I32, _I32, _P, _P]),
@@ -383,6 +384,24 @@ def debug_gemm_trace():
     tile = buf[n_step + n_dq:n_step + n_dq + n_tile].reshape(16, 32, 6)
     smid = buf[n_step + n_dq + n_tile:n_step + n_dq + n_tile + 16]
     return step, tile, smid, dq
+
+
+def debug_decode_trace():
+    """The decode gate_up kernel's per-tile phase trace of the last launch (a
+    library built with build.py --trace): (tile uint64 [16, 32, 10], cta uint64
+    [16, 2]) for CTAs 0, 19, ..., 285; tile fields: start ns, end ns, then SM
+    cycles of descriptor, set-up, columns, reduction + store, then q + 256 *
+    pairs, then the set-up's parts (issue, LUT wait + build, barrier); cta: SM
+    id + 1, exit ns.  Raises PWError (PW_ERR_NOT_BUILT) on a
+    library built without tracing."""
+    import numpy as np
+    need = ctypes.c_size_t(0)
+    lib().pw_debug_decode_trace(None, 0, ctypes.byref(need))
+    buf = np.zeros(need.value // 8, dtype=np.uint64)
+    _check(lib().pw_debug_decode_trace(buf.ctypes.data, buf.nbytes, None),
+           "pw_debug_decode_trace")
+    n_tile = 16 * 32 * 10
+    return buf[:n_tile].reshape(16, 32, 10), buf[n_tile:n_tile + 32].reshape(16, 2)
 
 
 def debug_index(planes, N, K, q, form, idx=None, stream=None):

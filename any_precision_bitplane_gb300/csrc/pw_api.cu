@@ -495,6 +495,19 @@ int pw_debug_gemm_trace(void* host, size_t bytes, size_t* needed) {
   return e == cudaSuccess ? PW_OK : cuda_fail(e, "trace copy");
 }
 
+int pw_debug_decode_trace(void* host, size_t bytes, size_t* needed) {
+  if (needed) *needed = pw::decode_trace_bytes();
+  if (host == nullptr || bytes < pw::decode_trace_bytes())
+    return fail(PW_ERR_INVALID_ARG, "host buffer NULL or smaller than %zu bytes",
+                pw::decode_trace_bytes());
+  int rc = pw::check_device();
+  if (rc) return rc;
+  cudaError_t e = cudaSuccess;
+  if (!pw::decode_trace_read(host, bytes, &e))
+    return fail(PW_ERR_NOT_BUILT, "libpw was built without the decode trace (build.py --trace)");
+  return e == cudaSuccess ? PW_OK : cuda_fail(e, "trace copy");
+}
+
 int pw_debug_index(const uint32_t* planes, int32_t N, int32_t K, int32_t q, int32_t form,
                    uint8_t* idx, cudaStream_t stream) {
   if (N < 0) return fail(PW_ERR_INVALID_ARG, "N < 0");

@@ -111,6 +111,86 @@ constexpr size_t kSmemBytes = kOffMisc + 64;
 // with register + immediate addressing.
 extern __shared__ __align__(16) unsigned char g_dsmem[];
 
+// ---------------------------------------------------------------- trace
+// With PW_TRACE (the traced build) the gate_up kernel records, for every
+// kDTraceStride-th CTA (up to kDTraceCtas of them) and its first kDTraceTiles
+// tiles: the tile's start and end (%globaltimer ns); the SM cycles (clock64)
+// that thread 0 spent on the slot descriptor (with the previous tile's
+// release), on the passes' set-up (LUT fetch, ring prime, table build, up to
+// the barrier after it), on the token groups' column loops (up to the barrier
+// after the partial sums) and on their reduction and h stores; the tile's q
+// and pair count; the set-up's parts (issuing the LUT loads and the first
+// ring copies; waiting for its LUT words and building its share of the
+// tables; the barrier after the build); and per traced CTA its SM and exit
+// time.  Thread 0 alone writes; misc[15] holds the current tile's record
+// index (-1: not traced).  The launch path clears the record before each
+// gate_up launch.  Without PW_TRACE every hook is empty.
+constexpr int kDTraceTiles = 32, kDTraceCtas = 16, kDTraceFields = 10;
+struct DecodeTrace {
+  // start ns, end ns, descriptor, set-up, columns, reduction + store (cycles),
+  // q + 256 * pairs, set-up parts: issue, LUT wait + build, barrier (cycles)
+  unsigned long long tile[kDTraceCtas][kDTraceTiles][kDTraceFields];
+  unsigned long long cta[kDTraceCtas][2];   // SM id + 1 (0: not traced), exit ns
+};
+#ifdef PW_TRACE
+constexpr int kDTraceStride = 19;
+__device__ DecodeTrace g_dtrace;
+__device__ __forceinline__ unsigned long long dtrace_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ int dtrace_cta() {
+  const int b = static_cast<int>(blockIdx.x);
+  return (b % kDTraceStride == 0 && b / kDTraceStride < kDTraceCtas) ? b / kDTraceStride : -1;
+}
+__device__ __forceinline__ unsigned long long* dtrace_field(int rec, int k) {
+  return &g_dtrace.tile[0][0][0] + static_cast<long long>(rec) * kDTraceFields + k;
+}
+#define PW_DTRACE_TILE_BEGIN(s, j, clk)                                                \
+  long long clk = 0;                                                                    \
+  if (threadIdx.x == 0) {                                                               \
+    const int c_ = dtrace_cta();                                                        \
+    (s).misc[15] = (c_ >= 0 && (j) < kDTraceTiles) ? c_ * kDTraceTiles + (j) : -1;      \
+    if ((s).misc[15] >= 0) {                                                            \
+      *dtrace_field((s).misc[15], 0) = dtrace_ns();                                     \
+      clk = clock64();                                                                  \
+    }                                                                                   \
+  }
+#define PW_DTRACE_MARK(clk) const long long clk = threadIdx.x == 0 ? clock64() : 0
+// a reduction (no value returned), so that thread 0 does not wait for the
+// record's old value
+#define PW_DTRACE_ADD(s, k, clk)                                                       \
+  do {                                                                                  \
+    if (threadIdx.x == 0 && (s).misc[15] >= 0)                                          \
+      atomicAdd(dtrace_field((s).misc[15], (k)),                                        \
+                static_cast<unsigned long long>(clock64() - (clk)));                    \
+  } while (0)
+#define PW_DTRACE_TILE_END(s, q, pairs)                                                \
+  do {                                                                                  \
+    if (threadIdx.x == 0 && (s).misc[15] >= 0) {                                        \
+      *dtrace_field((s).misc[15], 1) = dtrace_ns();                                     \
+      *dtrace_field((s).misc[15], 6) = (q) + 256ull * (pairs);                          \
+    }                                                                                   \
+  } while (0)
+#define PW_DTRACE_EXIT()                                                               \
+  do {                                                                                  \
+    const int c_ = dtrace_cta();                                                        \
+    if (threadIdx.x == 0 && c_ >= 0) {                                                  \
+      unsigned sm_;                                                                     \
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));                                  \
+      g_dtrace.cta[c_][0] = sm_ + 1ull;                                                 \
+      g_dtrace.cta[c_][1] = dtrace_ns();                                                \
+    }                                                                                   \
+  } while (0)
+#else
+#define PW_DTRACE_TILE_BEGIN(s, j, clk) do { } while (0)
+#define PW_DTRACE_MARK(clk) do { } while (0)
+#define PW_DTRACE_ADD(s, k, clk) do { } while (0)
+#define PW_DTRACE_TILE_END(s, q, pairs) do { } while (0)
+#define PW_DTRACE_EXIT() do { } while (0)
+#endif
+
 struct SmemPtrs {
   unsigned char* lut;
   unsigned char* ring;
@@ -756,6 +836,7 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
   const long long N = 2LL * a.I;
   int lo, hi;
   warp_range(KW, lo, hi);
+  PW_DTRACE_MARK(tr_cols);
   const char* xs[NT];
   gateup_xs<Q, NT>(a, w, ex, ent, g0, nt, xs);
   float2 acc[R][NT];
@@ -770,6 +851,8 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
     for (int g = 0; g < R; ++g)
       s.red[((warp * kTG + tk) * 2 + g) * 32 + lane] = acc[g][tk].x + acc[g][tk].y;
   __syncthreads();
+  PW_DTRACE_ADD(s, 4, tr_cols);
+  PW_DTRACE_MARK(tr_red);
   if (threadIdx.x < 32 * nt) {   // warp tk finishes token tk
     const int tk = threadIdx.x >> 5;
     float v0 = 0.f, v1 = 0.f;
@@ -785,12 +868,14 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
   }
   if (claim_counter && threadIdx.x == 0) s.misc[2] = claim;
   __syncthreads();
+  PW_DTRACE_ADD(s, 5, tr_red);
 }
 
 template <int Q, int R, bool COMPACT>
 __device__ void gateup_pass(const LayerArgs& a, const DecodeWs& w, const ExpertWork& ex,
                             const SlotInfo& ent, const PassRows<R>& pr, int hcol0,
                             const SmemPtrs& s, const BitConsts& bc, int* claim_counter) {
+  PW_DTRACE_MARK(tr_setup);
   __syncthreads();  // the previous pass is done with the LUT region and the rings
   // the LUT loads go out first, then the first token group's first columns
   // (whose activation rows need one more dependent load), so that both
@@ -800,8 +885,14 @@ __device__ void gateup_pass(const LayerArgs& a, const DecodeWs& w, const ExpertW
   const int nt0 = min(kTG, ex.ne);
   if (nt0 == 1) gateup_prime<Q, R, 1>(a, w, ex, ent, pr, 0, nt0);
   else gateup_prime<Q, R, kTG>(a, w, ex, ent, pr, 0, nt0);
+  PW_DTRACE_ADD(s, 7, tr_setup);
+  PW_DTRACE_MARK(tr_build);
   pass_lut_store<Q, R, COMPACT>(pl, a.status);
+  PW_DTRACE_ADD(s, 8, tr_build);
+  PW_DTRACE_MARK(tr_bar);
   __syncthreads();
+  PW_DTRACE_ADD(s, 9, tr_bar);
+  PW_DTRACE_ADD(s, 3, tr_setup);
   // token groups of one token take the one-token code; 2-4 tokens the kTG
   // code, with the missing tokens zero-filled (fewer code variants keep the
   // instruction cache warm)
@@ -856,9 +947,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerA
   // so the fence costs little.  The barriers since the tile's last h store
   // order every thread's stores before thread 0's fence.
   int pending = -1;
+#ifdef PW_TRACE
+  int tr_tiles = 0;
+#endif
   // A CTA's first tile is its block index; each tile claims the next one
   // from the counter (offset by the grid size) and leaves it in misc[2].
   for (int t = blockIdx.x; t < total;) {
+    PW_DTRACE_TILE_BEGIN(s, tr_tiles++, tr_desc);
     const int slot = t / tpe, x = t - slot * tpe;
     const SlotInfo si = w.routed_gu[slot];
     if (threadIdx.x == 0 && pending >= 0) {
@@ -873,6 +968,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerA
       }
       __syncthreads();
     } else {
+      PW_DTRACE_ADD(s, 2, tr_desc);   // the branch above waited for the descriptor
       const ExpertWork ex{si.e, si.off, si.ne};
       switch (si.q) {
         case 3: gateup_tile<3>(a, w, ex, si, x * kPairsPerTile, s, bc, counter); break;
@@ -882,6 +978,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerA
         default: gateup_tile<8>(a, w, ex, si, x * kPairsPerTile, s, bc, counter); break;
       }
       if (a.I <= kEarlyDownMaxI) pending = si.off;   // the down tiles wait per token group
+      PW_DTRACE_TILE_END(s, si.q, si.ne);
     }
     // claims only grow, so a tile id that does not advance ends the loop
     const int next = static_cast<int>(gridDim.x) + s.misc[2];
@@ -892,6 +989,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gateup_kernel(const LayerA
     __threadfence();
     atomicAdd(&w.gu_done[pending], 1);
   }
+  PW_DTRACE_EXIT();
 }
 
 // ---------------------------------------------------------------- down
@@ -1537,9 +1635,39 @@ cudaError_t launch_dequant_check(const uint32_t* planes, const uint16_t* lut, in
 int decode_max_pairs() { return kMaxPairs; }
 int decode_max_experts() { return kMaxExperts; }
 
+// The decode trace of the last gate_up launch (zeros where nothing was
+// recorded); returns false when tracing is compiled out.
+bool decode_trace_read(void* host, size_t bytes, cudaError_t* err) {
+#ifdef PW_TRACE
+  *err = cudaMemcpyFromSymbol(host, g_dtrace,
+                              sizeof(DecodeTrace) < bytes ? sizeof(DecodeTrace) : bytes);
+  return true;
+#else
+  (void)host;
+  (void)bytes;
+  *err = cudaSuccess;
+  return false;
+#endif
+}
+
+size_t decode_trace_bytes() { return sizeof(DecodeTrace); }
+
 namespace {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Clears the decode trace before a gate_up launch (nothing without PW_TRACE).
+cudaError_t decode_trace_clear(cudaStream_t stream) {
+#ifdef PW_TRACE
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_dtrace);
+  if (e != cudaSuccess) return e;
+  return cudaMemsetAsync(p, 0, sizeof(DecodeTrace), stream);
+#else
+  (void)stream;
+  return cudaSuccess;
+#endif
+}
 
 // Routed slots of a call: one per (expert, group of up to kTG pairs), so at
 // most the pairs, and at most E + P / kTG.
@@ -1695,6 +1823,7 @@ cudaError_t launch_decode(const LayerArgs& a, void* ws, cudaStream_t stream, boo
   }
 
   const BitConsts bc = make_bit_consts();
+  if ((e = decode_trace_clear(stream)) != cudaSuccess) return e;
   if ((e = record_timing(g_timing.before, stream)) != cudaSuccess) return e;
   e = launch_dependent(decode_gateup_kernel, dim3(gu_tiles < resident ? gu_tiles : resident),
                        dim3(kThreads), kSmemBytes, stream, a, w, bc);

@@ -161,5 +161,8 @@ cudaError_t launch_wait_check_mbar(int32_t* status, uint32_t polls, cudaStream_t
 // The GEMM trace (built with PW_TRACE): false when tracing is compiled out.
 bool gemm_trace_read(void* host, size_t bytes, cudaError_t* err);
 size_t gemm_trace_bytes();
+// The decode gate_up trace (built with PW_TRACE): false when compiled out.
+bool decode_trace_read(void* host, size_t bytes, cudaError_t* err);
+size_t decode_trace_bytes();
 
 }  // namespace pw

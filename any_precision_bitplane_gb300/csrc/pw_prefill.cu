@@ -146,7 +146,7 @@ extern __shared__ __align__(1024) unsigned char g_psmem[];
 // commit), the epilogue's start and end and the dequant warps' LUT load; and
 // the SM each traced CTA ran on.  The launch path clears the record before
 // each gate_up launch.  Without PW_TRACE every hook is empty.
-constexpr int kTraceSteps = 256, kTraceTiles = 32, kTraceCtas = 16, kTraceStride = 10;
+constexpr int kTraceSteps = 256, kTraceTiles = 32, kTraceCtas = 16;
 struct GemmTrace {
   unsigned long long step[kTraceCtas][kTraceSteps][4];   // ready, issued, dequantised, empty seen
   // per k-step and dequant warp of its set (8): the warp's wait for the
@@ -158,6 +158,7 @@ struct GemmTrace {
   unsigned long long smid[kTraceCtas];                   // SM id + 1 (0: CTA not traced)
 };
 #ifdef PW_TRACE
+constexpr int kTraceStride = 10;
 __device__ GemmTrace g_trace;
 __device__ __forceinline__ unsigned long long trace_now() {
   unsigned long long t;

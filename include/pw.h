@@ -419,25 +419,50 @@ int pw_debug_bounded_wait(pw_page_table* table, int32_t which, int32_t polls,
  * gate_up GEMM launches of both the prefill path and the decode path's heavy
  * experts, for CTAs 0, 10, 20, ... 150 (trace slot = block index / 10); the
  * record is cleared before each such launch, so it holds the last one.  This
- * call copies it (synchronously) into host memory laid out as
+ * call copies it (synchronously) into host memory laid out as, in this order,
  *   uint64 step[16][256][4]: for the CTA's first 256 k-steps (its ring
  *          position): [0] the MMA issuer found the stage full, [1] it had
  *          issued the stage's MMAs and commit, [2] a dequant set had written
  *          and announced the stage's A rows, [3] the token producer found the
  *          stage empty (0: not reached);
- *   uint64 tile[16][32][6]: for the CTA's first 32 tiles: [0] MMA start (the
- *          accumulator free), [1] last commit, [2] epilogue start, [3]
- *          epilogue end, [4] LUT load start, [5] LUT load end;
- *   uint64 smid[16]: the SM the CTA ran on, plus one (0: no such CTA);
  *   uint64 dq[16][256][8][4]: per k-step and warp of the dequant set that owns
  *          it: [0] the warp's wait for the stage's release done, [1] its
  *          announcement of the stage's A rows done, [2] its wait for the
- *          plane words done, [3] its index transpose done.
+ *          plane words done, [3] its index transpose done;
+ *   uint64 tile[16][32][6]: for the CTA's first 32 tiles: [0] MMA start (the
+ *          accumulator free), [1] last commit, [2] epilogue start, [3]
+ *          epilogue end, [4] LUT load start, [5] LUT load end;
+ *   uint64 smid[16]: the SM the CTA ran on, plus one (0: no such CTA).
  *   host    host buffer of at least *needed bytes
  *   needed  (may be NULL) receives the record's size
  * Errors: PW_ERR_INVALID_ARG (NULL or short buffer), PW_ERR_NOT_BUILT (built
  * without tracing), PW_ERR_UNSUPPORTED_DEVICE, PW_ERR_CUDA. */
 int pw_debug_gemm_trace(void* host, size_t bytes, size_t* needed);
+
+/* Per-tile phase trace of the decode gate_up kernel, a measurement hook with
+ * no counterpart on the pages.  A library built with tracing (build.py
+ * --trace) records, in each decode gate_up launch, for CTAs 0, 19, 38, ...
+ * 285 (trace slot = block index / 19) and their first 32 tiles, where thread
+ * 0 of the CTA spent its time; the record is cleared before each launch, so
+ * it holds the last one.  This call copies it (synchronously) into host
+ * memory laid out as, in this order,
+ *   uint64 tile[16][32][10]: [0] tile start and [1] tile end (%globaltimer
+ *          ns; 0: not reached); SM cycles (clock64) spent on [2] the slot
+ *          descriptor (with the release of the previous tile's h rows), [3]
+ *          the passes' set-up (LUT fetch, first copies of the ring, table
+ *          build), [4] the token groups' column loops up to the barrier after
+ *          the partial sums, [5] their reduction, SiLU and h stores; [6] the
+ *          tile's q + 256 * its number of pairs; the parts of [3]: [7]
+ *          issuing the LUT loads and first ring copies, [8] waiting for
+ *          thread 0's LUT words and building its share of the tables, [9]
+ *          the barrier after the build;
+ *   uint64 cta[16][2]: the SM the CTA ran on plus one (0: no such CTA), and
+ *          its exit time (ns).
+ *   host    host buffer of at least *needed bytes
+ *   needed  (may be NULL) receives the record's size
+ * Errors: PW_ERR_INVALID_ARG (NULL or short buffer), PW_ERR_NOT_BUILT (built
+ * without tracing), PW_ERR_UNSUPPORTED_DEVICE, PW_ERR_CUDA. */
+int pw_debug_decode_trace(void* host, size_t bytes, size_t* needed);
 
 /* ---- the fused layer without a workspace ------------------------------------
  * The PagedWeight pages have no counterpart to this entry point; it is a

@@ -67,9 +67,12 @@ def test_bounded_wait_rejects_bad_arguments(pw, dl):
         assert ei.value.code == pw.PW_ERR_INVALID_ARG
 
 
-def test_gemm_trace_needs_the_traced_build(pw):
-    # libpw.so is built without the GEMM trace: the reader says so and
-    # changes nothing (a traced library, build.py --trace, fills the record)
+def test_traces_need_the_traced_build(pw):
+    # libpw.so is built without the GEMM and decode traces: the readers say
+    # so and change nothing (a traced library, build.py --trace, fills them)
     with pytest.raises(pw.PWError) as e:
         pw.debug_gemm_trace()
+    assert e.value.code == pw.PW_ERR_NOT_BUILT
+    with pytest.raises(pw.PWError) as e:
+        pw.debug_decode_trace()
     assert e.value.code == pw.PW_ERR_NOT_BUILT

@@ -102,6 +102,15 @@ def test_ksplit_uniform_bitwidth(pw, q):
     check(pw, layer, "ksq%d" % q, 3)
 
 
+@pytest.mark.parametrize("q", [3, 4, 5, 6, 8])
+def test_long_gateup_k_uniform_bitwidth(pw, q):
+    # H = 4096: 16 word columns per warp in every gate_up pass, I = 96 a
+    # ragged last tile
+    layer = gen.make_layer(configs.custom("lk", 4096, 96, 4, 2, 5), seed=25)
+    layer = dataclasses.replace(layer, q=np.full_like(layer.q, q))
+    check(pw, layer, "lk%d" % q, 5)
+
+
 @pytest.mark.parametrize("T", [1, 4, 8])
 def test_qwen15_decode(pw, T):
     check(pw, host_layer("qwen15_decode"), "qwen15_decode", T)
