@@ -841,10 +841,12 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
   gateup_xs<Q, NT>(a, w, ex, ent, g0, nt, xs);
   float2 acc[R][NT];
   rows_dot<Q, R, NT, COMPACT>(ent.planes, N * KW, N, pr, lo, hi, xs, nt, s, bc, acc, primed);
-  // the tile's last group claims the CTA's next tile; the atomic's round
-  // trip overlaps the reduction and the epilogue
+  // the tile's last group claims the CTA's next tile from the last warp,
+  // which the reduction leaves idle (kTG < kWarps), so that no reducing warp
+  // waits for the atomic; its round trip overlaps the partial-sum stores and
+  // the reduction
   int claim = 0;
-  if (claim_counter && threadIdx.x == 0) claim = atomicAdd(claim_counter, 1);
+  if (claim_counter && threadIdx.x == 32 * (kWarps - 1)) claim = atomicAdd(claim_counter, 1);
 #pragma unroll
   for (int tk = 0; tk < NT; ++tk)
 #pragma unroll
@@ -865,8 +867,9 @@ __device__ void gateup_group(const LayerArgs& a, const DecodeWs& w, const Expert
     const int width = (R == 2) ? 32 : 16;
     const float h = lane < width ? v0 / (1.f + expf(-v0)) * v1 : 0.f;
     store_h(a, w, ex.off + g0 + tk, hcol0, width, lane, h, ent.q_other <= 4);
+  } else if (claim_counter && threadIdx.x == 32 * (kWarps - 1)) {
+    s.misc[2] = claim;
   }
-  if (claim_counter && threadIdx.x == 0) s.misc[2] = claim;
   __syncthreads();
   PW_DTRACE_ADD(s, 5, tr_red);
 }
