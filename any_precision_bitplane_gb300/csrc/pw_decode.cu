@@ -382,10 +382,12 @@ __device__ __forceinline__ void lut_store(const LutPieces<Q, R>& lp) {
 
 // Pair tables (Q = 3, 4): entry v = a + 16 b of a row holds the fp16 pair
 // {LUT[a], LUT[b]} (low half a), looked up by one byte of nibble indices.
-// kTPR threads build each row's table; thread c of a row fetches the row's
-// whole LUT (2^Q fp16 values, one or two 16-byte loads) and writes the
-// entries whose high nibble b is in its share.  Only pairs of valid indices
-// are written (Q = 3: a, b < 8).
+// kTPR threads build each row's table: lane L of warp W takes row L of slot
+// W % R and the share c = W / R of its entries (those whose high nibble b is
+// in that share), so that a warp's stores hit 32 different rows and banks,
+// and its fetches read 32 consecutive rows' LUTs (2^Q fp16 values each, one
+// or two 16-byte loads).  Only pairs of valid indices are written (Q = 3:
+// a, b < 8).
 template <int Q, int R>
 struct PairLutPieces {
   static constexpr int kTPR = 8 / R;                 // threads per row (R*32 rows)
@@ -399,8 +401,7 @@ __device__ __forceinline__ void pair_lut_fetch(const uint16_t* lut, const PassRo
                                                PairLutPieces<Q, R>& lp) {
   using L = PairLutPieces<Q, R>;
   if (threadIdx.x >= 256) return;   // 256 threads build the tables
-  const int rho = threadIdx.x / L::kTPR;
-  const int g = rho >> 5, lane = rho & 31;
+  const int g = (threadIdx.x >> 5) % R, lane = threadIdx.x & 31;
   const int row = seg_base<R>(pr, g, lane >> 4) + (lane & 15);
   const uint4* src = reinterpret_cast<const uint4*>(lut + static_cast<long long>(row) * (1 << Q));
 #pragma unroll
@@ -421,8 +422,7 @@ template <int Q, int R, bool COMPACT>
 __device__ __forceinline__ void pair_lut_store(const PairLutPieces<Q, R>& lp, int32_t* status) {
   using L = PairLutPieces<Q, R>;
   if (threadIdx.x >= 256) return;   // 256 threads build the tables
-  const int rho = threadIdx.x / L::kTPR, c = threadIdx.x % L::kTPR;
-  const int g = rho >> 5, lane = rho & 31;
+  const int g = (threadIdx.x >> 5) % R, c = (threadIdx.x >> 5) / R, lane = threadIdx.x & 31;
   bool bad = false;
 #pragma unroll
   for (int i = 0; i < L::kWords; ++i)
