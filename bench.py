@@ -91,6 +91,25 @@ def dist_env():
     return rank, world, local
 
 
+def slowest_rank_seconds(seconds, world, device=None):
+    """The job's time for a quantity each rank measured on its own: the
+    maximum over ranks (an all-reduce with MAX over the default process group
+    when world > 1; `device` is where the reduced tensor lives, the rank's GPU
+    under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return float(seconds)
+    import torch
+    t = torch.tensor([float(seconds)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, seconds, world, device=None):
+    """Whole-job throughput: the tokens of all ranks over the slowest rank's
+    time (weak scaling: each rank processes its own tokens_per_rank)."""
+    return tokens_per_rank * world / slowest_rank_seconds(seconds, world, device)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -534,14 +553,9 @@ def native(args):
         torch.distributed.barrier()
     time.sleep(0.2)
     sampler.stop()
-    ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
     T = args.T
-    tokens_total = T * args.steps * world
-    value = tokens_total / (ms / 1e3)
+    ms = slowest_rank_seconds(start.elapsed_time(stop) / 1e3, world, device) * 1e3
+    value = T * args.steps * world / (ms / 1e3)   # the slowest rank's time, all ranks' tokens
     per_launch_s = ms / 1e3 / args.steps
     achieved = step_bytes / per_launch_s / 1e9
 
@@ -555,7 +569,8 @@ def native(args):
     e2e = None
     if not args.no_e2e:
         e2e_dt, bi, bo = time_e2e(pw, cfg, layers, host, args.steps, args.warmup, device)
-        e2e = {"value": T * args.steps * world / e2e_dt, "unit": "tokens/s",
+        e2e = {"value": job_tokens_per_s(T * args.steps, e2e_dt, world, device),
+               "unit": "tokens/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "mode": "C ABI with pinned host buffers read/written by the kernels, K steps "
                        "in one CUDA graph, wall clock"}
