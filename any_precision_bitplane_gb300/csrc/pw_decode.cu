@@ -32,7 +32,10 @@
 //            share an SM with, so they wait for the whole gate_up grid.  The
 //            last tile to finish a 64-row range (arrival counter) forms
 //            out[t] = sum_j w_tj * y[t*k + j] over the range in j order, so
-//            the output is deterministic.
+//            the output is deterministic.  A long down K (I >= 8192) in a
+//            call whose down tiles fill less than two rounds is split in two
+//            halves (decode_down_kernel<2>): two tiles per range, the second
+//            half's partial sums in y2, which the combine adds first.
 //
 // Work inside a CTA: each lane owns one or two rows of the tile; the 8 warps
 // split the K columns and their partial sums meet in shared memory.  A warp
