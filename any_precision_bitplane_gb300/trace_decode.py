@@ -10,9 +10,9 @@ gate_up launch recorded for its CTAs 0, 19, ..., 285 (pw_debug_decode_trace):
                descriptor, the passes' set-up (LUT fetch, first ring copies,
                table build), the column loops and the reduction + h stores,
                and the median tile duration;
-  per CTA      tiles, first tile start and exit relative to the earliest
-               traced start, and the idle time from the CTA's exit to the last
-               traced exit (the launch's tail).
+  per CTA      tiles, exit relative to the earliest traced tile start, and
+               the idle time from the CTA's exit to the last traced exit (the
+               launch's tail).
 
 Run from the repository root:
   python -m any_precision_bitplane_gb300.trace_decode --workload qwen15_decode --T 4
@@ -24,6 +24,67 @@ import sys
 import numpy as np
 
 FIELDS = ("descriptor", "set-up", "columns", "reduction")
+CTA_STRIDE = 19   # traced CTAs: block index = CTA_STRIDE * trace slot
+
+
+def summarize(tile, cta):
+    """Medians of the record that pw_debug_decode_trace returns (tile uint64
+    [16, 32, 10], cta uint64 [16, 2]).  Returns a dict: `per_q` maps each
+    bitwidth to its traced tiles, the medians of the four phases (cycles),
+    of the set-up's three parts, of the pair count and of the tile duration
+    (us); `all` holds the same over every traced tile plus `shares` (each
+    phase's median over the sum of the four medians); `ctas` lists (CTA, SM,
+    tiles, exit us, idle us) per traced CTA, idle being the time from its exit
+    to the last traced exit; `span_us` runs from the first traced tile start
+    to that exit."""
+    tile = np.asarray(tile, dtype=np.int64)
+    cta = np.asarray(cta, dtype=np.int64)
+    done = (tile[:, :, 0] > 0) & (tile[:, :, 1] > 0)
+    q = tile[:, :, 6] & 255
+    pairs = tile[:, :, 6] >> 8
+    dur_us = (tile[:, :, 1] - tile[:, :, 0]) / 1e3
+
+    def stats(m):
+        med = [float(np.median(tile[:, :, 2 + f][m])) for f in range(4)]
+        return {"tiles": int(m.sum()), "phases": med,
+                "setup_parts": [float(np.median(tile[:, :, f][m])) for f in (7, 8, 9)],
+                "pairs": float(np.median(pairs[m])), "tile_us": float(np.median(dur_us[m]))}
+
+    out = {"per_q": {int(qq): stats(done & (q == qq)) for qq in sorted(set(q[done].tolist()))}}
+    out["all"] = stats(done)
+    tot = sum(out["all"]["phases"])
+    out["all"]["shares"] = [p / tot for p in out["all"]["phases"]]
+    t0 = tile[:, :, 0][tile[:, :, 0] > 0].min()
+    traced = np.nonzero(cta[:, 0] > 0)[0]
+    end = cta[traced, 1].max()
+    out["ctas"] = [(CTA_STRIDE * int(c), int(cta[c, 0]) - 1, int(done[c].sum()),
+                    (cta[c, 1] - t0) / 1e3, (end - cta[c, 1]) / 1e3) for c in traced]
+    out["span_us"] = (end - t0) / 1e3
+    return out
+
+
+def print_summary(sm):
+    print("%3s %6s %11s %9s %9s %10s %8s %10s" % ("q", "tiles", "descriptor", "set-up",
+                                                   "columns", "reduction", "pairs",
+                                                   "tile_us"))
+    rows = [("%3d" % qq, st) for qq, st in sm["per_q"].items()] + [("all", sm["all"])]
+    for label, st in rows:
+        ph = st["phases"]
+        print("%3s %6d %11.0f %9.0f %9.0f %10.0f %8.1f %10.2f" % (
+            label, st["tiles"], ph[0], ph[1], ph[2], ph[3], st["pairs"], st["tile_us"]))
+    print("shares of a median tile's thread-0 cycles: " + ", ".join(
+        "%s %.0f%%" % (FIELDS[f], 100.0 * sm["all"]["shares"][f]) for f in range(4)))
+    print("set-up parts per q (median cycles per tile, summed over its passes): "
+          "issue, LUT wait + table build, barrier")
+    for qq, st in sm["per_q"].items():
+        print("  q=%d: %s" % (qq, ", ".join("%.0f" % v for v in st["setup_parts"])))
+    print("%4s %4s %6s %9s %9s" % ("CTA", "SM", "tiles", "exit_us", "idle_us"))
+    for c, smid, n, ex, idle in sm["ctas"]:
+        print("%4d %4d %6d %9.2f %9.2f" % (c, smid, n, ex, idle))
+    idle = [c[4] for c in sm["ctas"]]
+    if idle:
+        print("traced span %.2f us; CTAs idle before the last exit: median %.2f us, max %.2f us"
+              % (sm["span_us"], float(np.median(idle)), float(np.max(idle))))
 
 
 def main():
@@ -61,61 +122,12 @@ def main():
                        path=pw.PATH_DECODE)
     torch.cuda.synchronize()
     tile, cta = pw.debug_decode_trace()
-    tile = tile.astype(np.int64)
-    cta = cta.astype(np.int64)
-
-    starts = tile[:, :, 0][tile[:, :, 0] > 0]
-    if starts.size == 0:
+    dl.close()
+    if not (tile[:, :, 0] > 0).any():
         raise SystemExit("no traced tile (is the call on the decode path?)")
-    t0 = starts.min()
     print("workload %s, T=%d: decode gate_up tiles of CTAs 0, 19, ..., 285 "
           "(SM cycles of thread 0; durations in us)" % (args.workload, args.T))
-    print("%3s %6s %11s %9s %9s %10s %8s %10s" % ("q", "tiles", "descriptor", "set-up",
-                                                   "columns", "reduction", "pairs",
-                                                   "tile_us"))
-    done = (tile[:, :, 1] > 0) & (tile[:, :, 0] > 0)
-    q = tile[:, :, 6] & 255
-    pairs = tile[:, :, 6] >> 8
-    allq = []
-    for qq in sorted(set(q[done].tolist())):
-        m = done & (q == qq)
-        med = [np.median(tile[:, :, 2 + f][m]) for f in range(4)]
-        dur = np.median((tile[:, :, 1] - tile[:, :, 0])[m]) / 1e3
-        print("%3d %6d %11.0f %9.0f %9.0f %10.0f %8.1f %10.2f" % (
-            qq, m.sum(), med[0], med[1], med[2], med[3], np.median(pairs[m]), dur))
-        allq.append(m)
-    m = done
-    med = [np.median(tile[:, :, 2 + f][m]) for f in range(4)]
-    tot = sum(med)
-    print("all %6d %11.0f %9.0f %9.0f %10.0f %8.1f %10.2f" % (
-        m.sum(), med[0], med[1], med[2], med[3], np.median(pairs[m]),
-        np.median((tile[:, :, 1] - tile[:, :, 0])[m]) / 1e3))
-    print("shares of a median tile's thread-0 cycles: " + ", ".join(
-        "%s %.0f%%" % (FIELDS[f], 100.0 * med[f] / tot) for f in range(4)))
-    print("set-up parts per q (median cycles per tile, summed over its passes): "
-          "issue, LUT wait + table build, barrier")
-    for qq in sorted(set(q[done].tolist())):
-        mq = done & (q == qq)
-        print("  q=%d: %s" % (qq, ", ".join("%.0f" % np.median(tile[:, :, f][mq])
-                                            for f in (7, 8, 9))))
-
-    exits = cta[:, 1][cta[:, 0] > 0]
-    end = exits.max() if exits.size else 0
-    print("%4s %4s %6s %10s %9s %9s" % ("CTA", "SM", "tiles", "start_us", "exit_us", "idle_us"))
-    idle = []
-    for c in range(cta.shape[0]):
-        if cta[c, 0] == 0:
-            continue
-        n = int(done[c].sum())
-        st = tile[c, 0, 0] - t0 if tile[c, 0, 0] > 0 else 0
-        ex = cta[c, 1] - t0
-        idle.append((end - cta[c, 1]) / 1e3)
-        print("%4d %4d %6d %10.2f %9.2f %9.2f" % (19 * c, cta[c, 0] - 1, n, st / 1e3, ex / 1e3,
-                                                    (end - cta[c, 1]) / 1e3))
-    if idle:
-        print("traced span %.2f us; CTAs idle before the last exit: median %.2f us, max %.2f us"
-              % ((end - t0) / 1e3, float(np.median(idle)), float(np.max(idle))))
-    dl.close()
+    print_summary(summarize(tile, cta))
 
 
 if __name__ == "__main__":
