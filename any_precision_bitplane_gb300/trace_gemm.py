@@ -24,6 +24,55 @@ import sys
 import numpy as np
 
 
+INTERVALS = ("kstep", "slack", "mma", "epi", "idle", "lut")
+
+
+def cta_intervals(s, t):
+    """One traced CTA's intervals (ns) from its k-step stamps s [steps, 4]
+    (issuer found full, issued, announced, producer found empty) and tile
+    stamps t [tiles, 6] (MMA start, last commit, epilogue start and end, LUT
+    load start and end); 0 marks a stamp not reached.  kstep: the issue
+    interval between consecutive issued k-steps, without the gaps that span a
+    tile boundary (more than 4 x the median: they hold the epilogue); slack:
+    how long an announced stage waited for the issuer; mma, epi, lut: per
+    tile; idle: from a tile's last commit to the next tile's MMA start."""
+    done = np.nonzero((s[:, 0] > 0) & (s[:, 1] > 0))[0]
+    rows = np.nonzero(t[:, 0] > 0)[0]
+    issued = set(done.tolist())
+    gaps = [int(s[i + 1, 1] - s[i, 1]) for i in done[:-1] if (i + 1) in issued]
+    out = {
+        "tiles": int(rows.size),
+        "slack": [int(s[i, 0] - s[i, 2]) for i in done if s[i, 2] > 0],
+        "mma": [int(t[j, 1] - t[j, 0]) for j in rows if t[j, 1] > 0],
+        "epi": [int(t[j, 3] - t[j, 2]) for j in rows if t[j, 2] > 0 and t[j, 3] > 0],
+        "idle": [int(t[j + 1, 0] - t[j, 1]) for j in rows
+                 if j + 1 < t.shape[0] and t[j + 1, 0] > 0 and t[j, 1] > 0],
+        "lut": [int(t[j, 5] - t[j, 4]) for j in rows if t[j, 4] > 0 and t[j, 5] > 0],
+    }
+    if out["mma"] and gaps:
+        cut = np.median(gaps) * 4
+        gaps = [g for g in gaps if g < cut]
+    out["kstep"] = gaps
+    return out
+
+
+def summarize(step, tile, smid, cta_stride=10):
+    """Per traced CTA (smid > 0): (CTA, SM, its intervals); and the medians of
+    each interval over all traced CTAs (None where none was recorded)."""
+    step = np.asarray(step, dtype=np.int64)
+    tile = np.asarray(tile, dtype=np.int64)
+    per_cta, agg = [], {k: [] for k in INTERVALS}
+    for c in range(step.shape[0]):
+        if smid[c] == 0:
+            continue
+        iv = cta_intervals(step[c], tile[c])
+        per_cta.append((cta_stride * c, int(smid[c]) - 1, iv))
+        for k in INTERVALS:
+            agg[k] += iv[k]
+    medians = {k: (float(np.median(v)) if v else None) for k, v in agg.items()}
+    return per_cta, medians
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="mixtral_prefill")
@@ -63,39 +112,19 @@ def main():
     tile = tile.astype(np.int64)
     print("workload %s, T=%d: gate_up GEMM stamps of CTAs 0, 10, ..., 150 (ns unless noted)"
           % (args.workload, args.T))
+    per_cta, medians = summarize(step, tile, smid)
     print("%4s %4s %6s %9s %9s %9s %9s %9s %9s %9s" %
           ("CTA", "SM", "tiles", "kstep_md", "kstep_p90", "slack_md", "mma_us", "epi_us",
            "idle_us", "lut_us"))
-    agg = {"kstep": [], "slack": [], "mma": [], "epi": [], "idle": [], "lut": []}
-    for c in range(step.shape[0]):
-        if smid[c] == 0:
-            continue
-        s = step[c]
-        done = np.nonzero((s[:, 0] > 0) & (s[:, 1] > 0))[0]
-        t = tile[c]
-        rows = np.nonzero(t[:, 0] > 0)[0]
-        # consecutive k-steps of one tile only (a tile boundary includes the epilogue wait)
-        gaps = [s[i + 1, 1] - s[i, 1] for i in done[:-1] if (i + 1) in set(done)]
-        slack = [s[i, 0] - s[i, 2] for i in done if s[i, 2] > 0]
-        mma = [t[j, 1] - t[j, 0] for j in rows if t[j, 1] > 0]
-        epi = [t[j, 3] - t[j, 2] for j in rows if t[j, 2] > 0 and t[j, 3] > 0]
-        idle = [t[j + 1, 0] - t[j, 1] for j in rows if j + 1 < t.shape[0] and t[j + 1, 0] > 0
-                and t[j, 1] > 0]
-        lut = [t[j, 5] - t[j, 4] for j in rows if t[j, 4] > 0 and t[j, 5] > 0]
-        # drop the k-step gaps that span a tile boundary (they hold the epilogue)
-        if mma:
-            cut = np.median(gaps) * 4 if gaps else 0
-            gaps = [g for g in gaps if g < cut]
-        for k, v in (("kstep", gaps), ("slack", slack), ("mma", mma), ("epi", epi),
-                     ("idle", idle), ("lut", lut)):
-            agg[k] += list(v)
 
-        def md(v, scale=1.0):
-            return "%9.1f" % (np.median(v) / scale) if len(v) else "%9s" % "-"
+    def md(v, scale=1.0):
+        return "%9.1f" % (np.median(v) / scale) if len(v) else "%9s" % "-"
+    for cta, sm, iv in per_cta:
+        gaps = iv["kstep"]
         print("%4d %4d %6d %s %s %s %s %s %s %s" % (
-            c * 10, smid[c] - 1, rows.size, md(gaps),
-            ("%9.1f" % np.percentile(gaps, 90)) if gaps else "%9s" % "-", md(slack),
-            md(mma, 1e3), md(epi, 1e3), md(idle, 1e3), md(lut, 1e3)))
+            cta, sm, iv["tiles"], md(gaps),
+            ("%9.1f" % np.percentile(gaps, 90)) if gaps else "%9s" % "-", md(iv["slack"]),
+            md(iv["mma"], 1e3), md(iv["epi"], 1e3), md(iv["idle"], 1e3), md(iv["lut"], 1e3)))
     if 0 <= args.dump < step.shape[0] and smid[args.dump]:
         s = step[args.dump]
         t0 = s[0, 0]
@@ -114,9 +143,8 @@ def main():
     print("all traced CTAs: k-step interval median %.0f ns; stage ready %.0f ns before the "
           "issuer reached it (median); tile MMA phase %.1f us, epilogue %.1f us, issuer idle "
           "between tiles %.1f us, LUT load %.1f us (medians)" % (
-              np.median(agg["kstep"]), np.median(agg["slack"]), np.median(agg["mma"]) / 1e3,
-              np.median(agg["epi"]) / 1e3, np.median(agg["idle"]) / 1e3,
-              np.median(agg["lut"]) / 1e3))
+              medians["kstep"], medians["slack"], medians["mma"] / 1e3, medians["epi"] / 1e3,
+              medians["idle"] / 1e3, medians["lut"] / 1e3))
 
 
 if __name__ == "__main__":
