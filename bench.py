@@ -71,6 +71,9 @@ def parse_args():
                     help="run only the prefill section and print its JSON")
     ap.add_argument("--prefill-tokens", type=int, default=0,
                     help="tokens of the prefill section (0: the workload's 4096)")
+    ap.add_argument("--uniform-q", type=int, default=0, choices=(0, 3, 4, 5, 6, 8),
+                    help="commit every block of the timed workload at this bitwidth "
+                         "(0: the workload's own mix); for per-bitwidth measurements")
     return ap.parse_args()
 
 
@@ -218,7 +221,8 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- native arm
 
-def setup_workload(name, T, device, copies=0):
+def setup_workload(name, T, device, copies=0, uniform_q=0):
+    import dataclasses
     import torch
     import any_precision_bitplane_gb300 as pw
     from any_precision_bitplane_gb300.layer import DeviceLayer
@@ -226,6 +230,8 @@ def setup_workload(name, T, device, copies=0):
 
     cfg = configs.config_by_name(name)
     layer = gen.make_layer(cfg, 0)
+    if uniform_q:   # every block committed at one bitwidth (a per-bitwidth measurement)
+        layer = dataclasses.replace(layer, q=np.full_like(layer.q, uniform_q))
     base = DeviceLayer(layer, device=device)
     tok = gen.make_tokens(layer, T)
     logits = torch.from_numpy(tok.logits).to(device)
@@ -532,7 +538,7 @@ def native(args):
     peak, peak_kind = measured_peaks()
 
     cfg, layer, layers, hidden, ids, wts, step_bytes, weight_bytes, host = \
-        setup_workload(args.workload, args.T, device, args.copies)
+        setup_workload(args.workload, args.T, device, args.copies, args.uniform_q)
     stream = torch.cuda.Stream(device)
     g, start, stop, out = time_device(pw, cfg, layers, hidden, ids, wts, args.steps,
                                       args.warmup, stream)
@@ -624,16 +630,21 @@ def native(args):
         "data": "synthetic (seeded codes, LUTs, bitwidths, hidden states and router logits)",
         "config": {"workload": "%s: H=%d I=%d E=%d top-%d, T=%d tokens per step" %
                                (cfg.name, cfg.H, cfg.I, cfg.E, cfg.k, T),
-                   "bitwidths": "q drawn per block from {3,4,5,6,8}",
-                   "l2": "inputs larger than L2: %d rotating layer copies, %.1f MB of routed "
-                         "weights per step" % (len(layers), weight_bytes / 1e6),
+                   "bitwidths": ("every block at q = %d" % args.uniform_q if args.uniform_q
+                                 else "q drawn per block from {3,4,5,6,8}"),
+                   "l2": ("inputs larger than L2: " if len(layers) * weight_bytes > L2_BYTES
+                          else "inputs fit in L2 (not HBM-bound): ") +
+                         "%d rotating layer copies, %.1f MB of routed weights per step" %
+                         (len(layers), weight_bytes / 1e6),
                    "timing": "CUDA events around one CUDA-graph replay of exactly K steps",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": dom_achieved, "peak": peak, "unit": "GB/s",
                      "frac": dom_achieved / peak, "peak_kind": peak_kind,
                      "kernel": "decode_gateup_kernel (gate_up + SiLU; the call's largest launch)",
                      "bytes_per_launch": gu_bytes, "ms_per_launch": dom_ms,
-                     "traffic": recorded_traffic("decode_gateup_kernel", args.workload, T)},
+                     # the recorded counters are of the workload's own bitwidth mix
+                     "traffic": (None if args.uniform_q else
+                                 recorded_traffic("decode_gateup_kernel", args.workload, T))},
         "call_roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                           "frac": achieved / peak,
                           "kernel": "whole pw_moe_forward decode call (prep, gate_up, down "
