@@ -81,6 +81,9 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kPairsPerTile = 32;   // gate_up tile: 32 gate rows + their 32 up rows
 constexpr int kDownRows = 64;       // down tile: two 32-row groups
 constexpr int kTG = 4;              // tokens per pass over the weights
+// the reduction of a token group uses warps 0..kTG-1, so the last warp is
+// free to claim the next gate_up tile meanwhile
+static_assert(kTG < kWarps, "the claiming warp must not reduce");
 constexpr int kStages = 3;          // per-warp cp.async ring depth (word columns)
 constexpr int kMaxPairs = 4096;     // T*k limit of this path
 constexpr int kMaxExperts = 1024;
